@@ -1,0 +1,480 @@
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step is one decode layer-step of the whole hot path: pa_store_kv (the step's new K/V rows
+into the pool) then pa_decode (split-K paged GQA decode + merge), over the
+``qwen3_06b_decode`` workload (256 sequences, contexts U[100, 4096], 16/8 heads, D 128,
+256-token blocks, bf16). Two layers' pools are used in turn so that consecutive steps read
+different data; each pool (2.7 GB) is far larger than the 129 MB L2.
+
+Headline: KV bytes the step must read (every cached row of K and V once per kv head) divided
+by the device time of the step, in GB/s, and as a fraction of the measured HBM peak; decode
+steps per second per layer. The same line carries:
+
+* ``roofline``: the pa_decode call (split kernel + merge) timed alone with CUDA events inside
+  the timed region, against the measured copy bandwidth;
+* ``e2e``: the same metric when every step also copies its inputs from pinned host memory and
+  reads the output back, synchronising each step (the pool stays resident, as in an engine);
+* ``cpu_baseline``: the fp64 CPU oracle on a bounded sample of the same workload, on the
+  host's cores;
+* ``rows``: the other rows of the path measured the same way: the store alone, and the
+  varlen prefill with a 512-token cached prefix (``prefill_prefix``) with its store.
+
+``--impl reference`` times the CPU oracle as the reference arm, on the same metric.
+Multi-GPU (torchrun): every rank runs an independent replica (the path shards by sequence
+with no exchange), value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged-decode KV-read GB/s (% of GB300 HBM peak); decode steps/sec per layer"
+DEFAULT_WORKLOAD = "qwen3_06b_decode"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic of one decode_split_kernel launch on the default workload, from the ncu capture
+# summarised in profiles/ (scaled as described there); valid only for the decode source it was
+# taken on, identified by its hash.
+DECODE_TRAFFIC = {"sha256": None, "bytes": None}
+
+
+def peaks() -> tuple[dict, str]:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        return json.loads(p.read_text()), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kv_bytes(context_lens, Hkv, D, elem=2) -> int:
+    return int(np.asarray(context_lens, np.int64).sum()) * Hkv * D * 2 * elem
+
+
+def prefill_flops(q_lens, k_lens, Hq, D) -> int:
+    tot = 0
+    for ql, kl in zip(np.asarray(q_lens, np.int64), np.asarray(k_lens, np.int64)):
+        P = int(kl - ql)
+        tot += 4 * Hq * D * (int(ql) * P + int(ql) * (int(ql) + 1) // 2)
+    return tot
+
+
+def src_hash(name: str) -> str:
+    return hashlib.sha256((ROOT / "paged_kv_cache_83_gb300" / "csrc" / name).read_bytes()).hexdigest()
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU is busy."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in Path(self.path).read_text().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                             "sw_power": parts[8]})
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in busy):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(busy),
+                "power_w_median": statistics.median(r["power"] for r in busy)}
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle timing (the baseline and the reference arm)
+# ---------------------------------------------------------------------------------------------
+
+def oracle_decode_rate(case, budget_s: float = 12.0, threads: int = 0) -> dict:
+    """Time the oracle's decode on a bounded sample of the case's sequences (after applying the
+    step's store, as the GPU step does), growing the sample until ~budget_s of work."""
+    import oracle
+    orc = oracle.get()
+    threads = threads or (os.cpu_count() or 1)
+    kc, vc = orc.store_kv(case.k_new, case.v_new, case.k_cache, case.v_cache, case.slot_mapping)
+    order = np.random.default_rng(123).permutation(case.B)
+    n = min(case.B, 2)
+    while True:
+        rows = np.sort(order[:n])
+        t = time.perf_counter()
+        orc.decode(case.q[rows], kc, vc, case.block_tables[rows], case.context_lens[rows],
+                   scale=case.scale, dtype=case.dtype, threads=threads)
+        dt = time.perf_counter() - t
+        if dt >= budget_s / 4 or n == case.B:
+            break
+        n = min(case.B, max(n + 1, int(n * min(8.0, (budget_s / 4) / max(dt, 1e-3)))))
+    nbytes = kv_bytes(case.context_lens[rows], case.Hkv, case.D)
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": orc.max_threads(), "kind": "oracle",
+            "sample": f"{n} of {case.B} sequences of {case.name} (store applied, fp64 decode), "
+                      f"{nbytes / 1e6:.1f} MB of KV in {dt:.2f} s",
+            "seconds": dt, "seqs": int(n), "rows": rows}
+
+
+def run_reference(args, ws_, rank):
+    if rank != 0:
+        return
+    case = W.make(args.workload)
+    probe = oracle_decode_rate(case, budget_s=4.0)
+    rows = probe["rows"]
+    import oracle
+    orc = oracle.get()
+    kc, vc = orc.store_kv(case.k_new, case.v_new, case.k_cache, case.v_cache, case.slot_mapping)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t = time.perf_counter()
+        orc.decode(case.q[rows], kc, vc, case.block_tables[rows], case.context_lens[rows],
+                   scale=case.scale, dtype=case.dtype, threads=os.cpu_count() or 1)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t)
+    nbytes = kv_bytes(case.context_lens[rows], case.Hkv, case.D)
+    tot = sum(times)
+    value = nbytes * len(times) / tot / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws_,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, "seqs_per_step": len(rows)},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle",
+                             "cores": orc.max_threads(),
+                             "sample": f"{len(rows)} of {case.B} sequences of {case.name} per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------------
+
+def to_dev(torch, bits, dt, dev):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev)
+    return t.view(torch.float16 if dt == "f16" else torch.bfloat16)
+
+
+class DecodeLayer:
+    def __init__(self, torch, pa, case, dev):
+        self.c = case
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+        self.kc = to_dev(torch, case.k_cache, case.dtype, dev)
+        self.vc = to_dev(torch, case.v_cache, case.dtype, dev)
+        self.q = to_dev(torch, case.q, case.dtype, dev)
+        self.k_new = to_dev(torch, case.k_new, case.dtype, dev)
+        self.v_new = to_dev(torch, case.v_new, case.dtype, dev)
+        self.bt, self.cl, self.sm = i32(case.block_tables), i32(case.context_lens), i32(case.slot_mapping)
+        n = pa.pa_decode_workspace_size(case.B, case.Hq, case.Hkv, case.D, case.max_blocks_per_seq,
+                                        case.block_size)
+        self.ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+        self.out = torch.empty_like(self.q)
+
+
+def run_gpu(args, ws_, rank, local):
+    import torch
+    import paged_kv_cache_83_gb300 as pa
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pa.load()
+    stream = torch.cuda.current_stream()
+    pk, pk_kind = peaks()
+    hbm = float(pk["hbm_gbs"])
+    bf16_peak = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+
+    # ---- inputs: two layers of the decode workload (seeds differ per layer and rank) ----
+    base = W.CONFIGS[args.workload].seed
+    layers = [DecodeLayer(torch, pa, W.make(args.workload, seed=base + 1000 * rank + l), dev)
+              for l in range(args.layers)]
+    c0 = layers[0].c
+    nbytes = [kv_bytes(L.c.context_lens, L.c.Hkv, L.c.D) for L in layers]
+    nl = len(layers)
+    plan_splits = pa.pa_decode_workspace_size(c0.B, c0.Hq, c0.Hkv, c0.D, c0.max_blocks_per_seq,
+                                              c0.block_size) > 0
+    launches_per_step = 2 + (1 if plan_splits else 0)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    dec_ev = [(ev(), ev()) for _ in range(args.steps)]
+    st_ev = [(ev(), ev()) for _ in range(args.steps)]
+
+    def step(i, timed=False):
+        L = layers[i % nl]
+        if timed:
+            st_ev[i][0].record(stream)
+        pa.pa_store_kv(L.k_new, L.v_new, L.kc, L.vc, L.sm)
+        if timed:
+            st_ev[i][1].record(stream)
+            dec_ev[i][0].record(stream)
+        pa.pa_decode(L.out, L.q, L.kc, L.vc, L.bt, L.cl, L.c.scale, workspace=L.ws)
+        if timed:
+            dec_ev[i][1].record(stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for i in range(args.warmup):
+        step(i)
+    clocks = Clocks(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    t0, t1 = ev(), ev()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i, timed=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    # keep the GPU busy ~1 s more with the same step so the clock sampler sees it under load
+    t_end = time.perf_counter() + (0.0 if args.no_clock_tail else 1.0)
+    j = 0
+    while time.perf_counter() < t_end:
+        step(j)
+        j += 1
+        if j % 64 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+
+    elapsed = t0.elapsed_time(t1)  # ms
+    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
+    st_ms = [a.elapsed_time(b) for a, b in st_ev]
+    if dist is not None:
+        tt = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed = float(tt.item())
+    ms_step = elapsed / args.steps
+    step_bytes = sum(nbytes[i % nl] for i in range(args.steps))
+    value = ws_ * step_bytes / (elapsed * 1e-3) / 1e9
+    dec_mean = statistics.mean(dec_ms)
+    dec_bytes_mean = statistics.mean(nbytes[i % nl] for i in range(args.steps))
+    achieved = dec_bytes_mean / (dec_mean * 1e-3) / 1e9
+    dsha = src_hash("decode.cu")
+    traffic = DECODE_TRAFFIC["bytes"] if DECODE_TRAFFIC["sha256"] == dsha else None
+
+    # ---- e2e: inputs from pinned host memory each step, output read back each step ----
+    L = layers[0]
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = [pin(x) for x in (L.q, L.k_new, L.v_new, L.sm, L.bt, L.cl)]
+    d_in = [torch.empty_like(x) for x in (L.q, L.k_new, L.v_new, L.sm, L.bt, L.cl)]
+    h_out = torch.empty(L.out.shape, dtype=L.out.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    d2h = h_out.numel() * h_out.element_size()
+    e_steps = 0 if args.no_e2e else max(1, min(args.steps, 200))
+
+    def e2e_step():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        q, kn, vn, sm, bt, cl = d_in
+        pa.pa_store_kv(kn, vn, L.kc, L.vc, sm)
+        pa.pa_decode(L.out, q, L.kc, L.vc, bt, cl, L.c.scale, workspace=L.ws)
+        h_out.copy_(L.out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3 if e_steps else 0):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        tt = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e_ms = float(tt.item())
+    e2e_value = ws_ * nbytes[0] * e_steps / (e_ms * 1e-3) / 1e9 if e_steps else None
+
+    # ---- other rows: prefill with a cached prefix (store + varlen prefill) ----
+    rows = {}
+    if not args.skip_prefill:
+        rows.update(bench_prefill(torch, pa, dev, stream, bf16_peak, hbm, args))
+    st_mean = statistics.mean(st_ms)
+    st_bytes = 4 * c0.B * c0.Hkv * c0.D * 2
+    rows["store_kv_decode"] = {"kernel": "store_kv_kernel", "ms": st_mean,
+                               "GB_per_s": st_bytes / (st_mean * 1e-3) / 1e9,
+                               "bytes": st_bytes, "note": "256 new rows: launch-latency bound"}
+    rows["decode"] = {"kernel": "decode_split_kernel + decode_merge_kernel", "ms": dec_mean,
+                      "GB_per_s": achieved, "frac_of_hbm": achieved / hbm}
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        r = oracle_decode_rate(layers[0].c)
+        r.pop("rows")
+        r.pop("seqs")
+        cpu = r
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws_, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": c0.dtype, "data": "synthetic",
+        "config": {"workload": args.workload, "seqs": c0.B, "Hq": c0.Hq, "Hkv": c0.Hkv,
+                   "D": c0.D, "block_size": c0.block_size,
+                   "kv_bytes_per_step": int(statistics.mean(nbytes)),
+                   "layers_rotated": nl,
+                   "l2": f"inputs larger than L2: each step reads a {statistics.mean(nbytes) / 1e9:.1f} GB "
+                         f"KV set of its own layer ({nl} layers alternate)",
+                   "parallelism": f"replicas x{ws_}" if ws_ > 1 else "single GPU"},
+        "pct_of_hbm_peak": 100.0 * value / hbm / ws_,
+        "decode_steps_per_sec_per_layer": 1e3 / ms_step,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "kernel": "pa_decode: decode_split_kernel + decode_merge_kernel",
+                     "peak_source": f"{pk_kind} hbm_gbs"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e_steps,
+                "note": "pool resident; per step: H2D of q, new K/V, slots, tables, lengths; "
+                        "store + decode; D2H of the output; stream sync"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "rows": rows,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def bench_prefill(torch, pa, dev, stream, bf16_peak, hbm, args) -> dict:
+    c = W.make("prefill_prefix")
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+    kc, vc = to_dev(torch, c.k_cache, c.dtype, dev), to_dev(torch, c.v_cache, c.dtype, dev)
+    k, v, q = (to_dev(torch, x, c.dtype, dev) for x in (c.k, c.v, c.q))
+    sm, cq, ck, bt = i32(c.slot_mapping), i32(c.cu_seqlens_q), i32(c.cu_seqlens_k), i32(c.block_tables)
+    out = torch.empty_like(q)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > L2
+
+    def run(timed_evs=None):
+        if timed_evs:
+            timed_evs[0].record(stream)
+        pa.pa_store_kv(k, v, kc, vc, sm)
+        if timed_evs:
+            timed_evs[1].record(stream)
+        pa.pa_prefill_varlen(out, q, None, None, kc, vc, cq, ck, c.max_seqlen_q, c.max_seqlen_k, bt,
+                             Hkv=c.Hkv, scale=c.scale)
+        if timed_evs:
+            timed_evs[2].record(stream)
+
+    for _ in range(3):
+        run()
+    n = max(3, min(args.steps, 50))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    torch.cuda.synchronize()
+    for e in evs:
+        flush.zero_()  # L2 flush between iterations (outside the events)
+        run(e)
+    torch.cuda.synchronize()
+    st = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    pf = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    flops = prefill_flops(c.q_lens, c.k_lens, c.Hq, c.D)
+    st_bytes = 4 * int(c.q.shape[0]) * c.Hkv * c.D * 2
+    return {"prefill": {"workload": "prefill_prefix", "kernel": "prefill_mma_kernel",
+                        "ms": pf, "TFLOP_per_s": flops / (pf * 1e-3) / 1e12,
+                        "frac_of_bf16_peak": flops / (pf * 1e-3) / 1e12 / bf16_peak,
+                        "peak": bf16_peak, "flops": flops, "l2": "flushed between iterations"},
+            "store_kv_prefill": {"kernel": "store_kv_kernel", "ms": st, "bytes": st_bytes,
+                                 "GB_per_s": st_bytes / (st * 1e-3) / 1e9,
+                                 "frac_of_hbm": st_bytes / (st * 1e-3) / 1e9 / hbm}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=[k for k, w in W.CONFIGS.items() if w.kind == "decode"])
+    ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--layers", type=int, default=2, help="layers whose pools alternate")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clock-tail", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws_, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws_, rank)
+        return
+    run_gpu(args, ws_, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,174 @@
+/*
+ * pa.h: C ABI of the paged KV-cache hot path (store, paged decode, varlen prefill) for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The three operations are the attention layer's GPU work in the engines that the
+ * "nano-vLLM Part 4" page (section 3, the prefill/decode table and the per-rank tensor list)
+ * and the smzdm nano-vLLM deep dive ("模型实现细节": store_kvcache, flash_attn_varlen_func,
+ * flash_attn_with_kvcache, the prefix-cache rule) describe, and that the "mini-vLLM" page
+ * describes for its 16-token paged pool with grouped-query attention.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers are DEVICE pointers unless a comment says otherwise. The caller owns every
+ *   buffer. The library allocates nothing that outlives a call. Nothing is freed by the library.
+ * - Every call is asynchronous on `stream`; it returns after the launch. Errors that the host
+ *   can see are returned before anything is launched, and nothing is written then.
+ * - Element types: `pa_dtype` selects fp16 or bf16 for q, k, v, the pools and the output.
+ *   Scores, softmax and accumulation run in fp32; the output is rounded once (to nearest even).
+ * - Pools: `k_cache` and `v_cache` are each [num_blocks, block_size, Hkv, D], contiguous.
+ *   Token slot `s` (0 <= s < num_blocks * block_size) is block `s / block_size`, offset
+ *   `s % block_size`; its K row for kv head g starts at element (s * Hkv + g) * D.
+ * - Block tables: int32 [rows, max_blocks_per_seq], row-major; entry b of a row is the physical
+ *   block holding that sequence's positions b*block_size .. b*block_size + block_size - 1.
+ *   Only the first ceil(length / block_size) entries of a row are read; the rest may hold
+ *   anything (the workloads use -1).
+ * - Grouped-query heads: query head h reads kv head h / (Hq / Hkv).
+ * - Alignment: every tensor pointer must be 16-byte aligned (torch allocations are).
+ * - Supported: D = 64 or 128 (pa_store_kv: any D with D % 8 == 0); 1 <= Hq / Hkv <= 8 with
+ *   Hq % Hkv == 0; any block_size >= 1.
+ * - `err` (nullable, device int32): data-dependent problems that only the GPU sees are OR-ed
+ *   into *err as PA_DEVERR_* bits and the offending item is skipped, with every memory
+ *   access kept in bounds. The library never traps and never clears *err: zero it before the call if you
+ *   want to read it afterwards.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_NULL = 1,        /* a required pointer is NULL */
+    PA_ERR_SHAPE = 2,       /* a size is negative, zero where it must not be, or inconsistent */
+    PA_ERR_DTYPE = 3,       /* dtype is not PA_F16 or PA_BF16 */
+    PA_ERR_UNSUPPORTED = 4, /* a shape outside the supported set (D, group size, alignment) */
+    PA_ERR_WORKSPACE = 5,   /* workspace missing or smaller than pa_decode_workspace_size() */
+    PA_ERR_CUDA = 6         /* a CUDA runtime call failed (e.g. the launch) */
+} pa_status;
+
+typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits OR-ed into *err by the kernels. */
+#define PA_DEVERR_SLOT 1   /* slot_mapping entry >= num_blocks * block_size: token not stored */
+#define PA_DEVERR_TABLE 2  /* a block-table entry that must be read lies outside [0, num_blocks):
+                              the positions of that block are left out of the softmax */
+#define PA_DEVERR_LENGTH 4 /* a context length or cu_seqlens span outside its contract
+                              (negative, longer than the block table covers, k_len < q_len,
+                              q_len > max_seqlen_q): the sequence's output rows are zero */
+
+/*
+ * pa_store_kv: scatter this step's new K and V rows into the pools.
+ *
+ * Source: "nano-vLLM Part 4" section 3 (table row "K/V work": K/V written for every new prompt
+ * token in prefill, for one input token per sequence in decode; step 3: per-rank slot
+ * mappings); smzdm deep dive "模型实现细节" (store_kvcache writes newly computed K and V rows
+ * to their physical positions).
+ *
+ *   for t in [0, T): s = slot_mapping[t]; if s < 0 skip (padding token)
+ *       k_cache row s = k[t]  (Hkv * D elements, bit copy);  v_cache row s = v[t]
+ *
+ * k, v          [T, Hkv, D] contiguous, the new rows.
+ * k_cache/v_cache  pools (see above), written in place.
+ * slot_mapping  int32 [T]; entries must be unique among the non-negative ones (two tokens in
+ *               one slot leave either row there). An entry >= num_blocks * block_size sets
+ *               PA_DEVERR_SLOT and that token is not stored.
+ * T == 0 is a no-op. Bytes moved: 4 * T * Hkv * D * 2 (read k, v; write both pools).
+ */
+pa_status pa_store_kv(const void *k, const void *v, void *k_cache, void *v_cache,
+                      const int32_t *slot_mapping, int T, int num_blocks, int block_size, int Hkv,
+                      int D, pa_dtype dtype, int32_t *err, cudaStream_t stream);
+
+/*
+ * pa_decode_workspace_size: bytes of scratch pa_decode needs for these sizes on the current
+ * device (split-K partial results: per (sequence, query head, split) D fp32 values plus the
+ * running max and sum). 0 means no scratch is needed. Never fails; returns 0 for sizes that
+ * pa_decode would reject.
+ */
+size_t pa_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_blocks_per_seq,
+                                int block_size);
+
+/*
+ * pa_decode: paged grouped-query decode attention, one query token per sequence.
+ *
+ * Source: "nano-vLLM Part 4" section 3 (decode: one already-sampled token per sequence;
+ * attention over cached history through a block table, flash_attn_with_kvcache); "mini-vLLM"
+ * (one token per sequence attending to that sequence's cached keys and values; grouped-query
+ * attention).
+ *
+ *   for sequence i, query head h, kv head g = h / (Hq / Hkv), n = context_lens[i]:
+ *       s_j = scale * q[i,h,:] . K_j,   K_j, V_j = row j of sequence i (0 <= j < n) via its table
+ *       out[i,h,:] = sum_j softmax(s)_j V_j         (zeros when n == 0)
+ *
+ * The step's own token must already be in the pool (pa_store_kv first) and counted in n.
+ *
+ * out           [B, Hq, D], written.
+ * q             [B, Hq, D].
+ * block_tables  int32 [B, max_blocks_per_seq].
+ * context_lens  int32 [B]; 0 <= n <= max_blocks_per_seq * block_size, else PA_DEVERR_LENGTH.
+ * scale         softmax scale (1/sqrt(D) in the usual case).
+ * workspace     device scratch of at least pa_decode_workspace_size(B, Hq, Hkv, D,
+ *               max_blocks_per_seq, block_size) bytes, or NULL when that size is 0. Its
+ *               contents on entry do not matter; calls that share a workspace must not overlap
+ *               on the GPU.
+ * B == 0 is a no-op.
+ */
+pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *context_lens, int B, int Hq, int Hkv, int D, int block_size,
+                    int num_blocks, float scale, pa_dtype dtype, void *workspace,
+                    size_t workspace_bytes, int32_t *err, cudaStream_t stream);
+
+/*
+ * pa_prefill_varlen: variable-length (causal) prefill attention over packed prompts, with a
+ * cached prefix read from the pool.
+ *
+ * Source: "nano-vLLM Part 4" section 3 (prefill: packed tokens, variable-length attention,
+ * optional prefix block table); smzdm deep dive "GPU执行优化" (cu_seqlens mark sequence
+ * boundaries) and "模型实现细节" (the prefix cache is used when cu_seqlens_k > cu_seqlens_q);
+ * "mini-vLLM" (concatenated prompts, each attending causally to itself).
+ *
+ *   for sequence s: q_len = cu_seqlens_q[s+1] - cu_seqlens_q[s],
+ *                   k_len = cu_seqlens_k[s+1] - cu_seqlens_k[s],  P = k_len - q_len >= 0
+ *   new row r (0 <= r < q_len) sits at position P + r and, with `causal`, sees keys 0 .. P + r
+ *   (without it, all k_len keys):
+ *       out[cu_seqlens_q[s] + r, h, :] = sum_j softmax_j(scale * q . K_j) V_j
+ *
+ * Key/value source:
+ *   block_tables != NULL: every key (prefix and new) is read from k_cache / v_cache through
+ *       block_tables[s]; call pa_store_kv for the new rows first. k and v are not read (may
+ *       be NULL).
+ *   block_tables == NULL: keys are the packed rows k[cu_seqlens_k[s] + j], v[...] ([Tk, Hkv, D],
+ *       Tk = cu_seqlens_k[S]); k_cache, v_cache are not read (may be NULL).
+ *
+ * out           [Tq, Hq, D], Tq = cu_seqlens_q[S], written (rows of sequences flagged with
+ *               PA_DEVERR_LENGTH are zero).
+ * q             [Tq, Hq, D].
+ * cu_seqlens_q, cu_seqlens_k  int32 [S+1], non-decreasing, starting at 0.
+ * max_seqlen_q  host int >= every q_len (sizes the grid); max_seqlen_k is accepted for
+ *               interface parity and not needed.
+ * S == 0 is a no-op.
+ */
+pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void *v,
+                            const void *k_cache, const void *v_cache,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int S,
+                            int max_seqlen_q, int max_seqlen_k, const int32_t *block_tables,
+                            int max_blocks_per_seq, int Hq, int Hkv, int D, int block_size,
+                            int num_blocks, float scale, int causal, pa_dtype dtype,
+                            int32_t *err, cudaStream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char *pa_status_string(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,164 @@
+"""Python binding of the C ABI in ``include/pa.h`` (argument marshalling only).
+
+Each function takes torch CUDA tensors, checks their dtype / shape / contiguity, and calls the
+entry point of the same name in ``_build/libpagedattn.so`` with raw device pointers and the
+current CUDA stream. Every step of the computation runs in the library's kernels; there is no
+fallback: if the library is missing or a call fails, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+PKG = Path(__file__).resolve().parent
+LIB_PATH = PKG / "_build" / "libpagedattn.so"
+
+PA_F16, PA_BF16 = 0, 1
+PA_DEVERR_SLOT, PA_DEVERR_TABLE, PA_DEVERR_LENGTH = 1, 2, 4
+EXPORTS = ("pa_store_kv", "pa_decode_workspace_size", "pa_decode", "pa_prefill_varlen",
+           "pa_status_string")
+
+_lib = None
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: status {status} ({status_string(status)})")
+        self.status = status
+
+
+def load(path: Path | str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library once (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = Path(path)
+    if not path.exists():
+        raise RuntimeError(f"{path} is missing: build it with paged_kv_cache_83_gb300.build.build()")
+    lib = ctypes.CDLL(str(path))
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.pa_store_kv.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
+    lib.pa_store_kv.restype = I
+    lib.pa_decode_workspace_size.argtypes = [I, I, I, I, I, I]
+    lib.pa_decode_workspace_size.restype = Z
+    lib.pa_decode.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, P, Z, P, P]
+    lib.pa_decode.restype = I
+    lib.pa_prefill_varlen.argtypes = [P, P, P, P, P, P, P, P, I, I, I, P, I, I, I, I, I, I, F, I,
+                                      I, P, P]
+    lib.pa_prefill_varlen.restype = I
+    lib.pa_status_string.argtypes = [I]
+    lib.pa_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().pa_status_string(int(status)).decode()
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return PA_F16
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _i32(t: torch.Tensor | None, name: str):
+    if t is not None and t.dtype != torch.int32:
+        raise TypeError(f"{name} must be int32")
+    return _ptr(t)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise PagedAttnError(fn, status)
+
+
+def pa_store_kv(k, v, k_cache, v_cache, slot_mapping, err=None, stream=None) -> None:
+    """Scatter k, v [T, Hkv, D] into k_cache, v_cache [NB, bs, Hkv, D] at slot_mapping [T]."""
+    NB, bs, Hkv, D = k_cache.shape
+    T = k.shape[0]
+    if tuple(k.shape) != (T, Hkv, D) or tuple(v.shape) != (T, Hkv, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch")
+    if slot_mapping.shape != (T,):
+        raise ValueError("slot_mapping must be [T]")
+    dt = _dtype(k_cache)
+    if k.dtype != k_cache.dtype or v.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise TypeError("k, v and the pools must share a dtype")
+    _check("pa_store_kv", load().pa_store_kv(
+        _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _i32(slot_mapping, "slot_mapping"), T, NB,
+        bs, Hkv, D, dt, _i32(err, "err"), _stream(stream)))
+
+
+def pa_decode_workspace_size(B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int,
+                             block_size: int) -> int:
+    """Bytes of scratch pa_decode needs on the current device for these sizes."""
+    return int(load().pa_decode_workspace_size(B, Hq, Hkv, D, max_blocks_per_seq, block_size))
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+              workspace=None, err=None, stream=None) -> None:
+    """Paged GQA decode: out [B, Hq, D] from q [B, Hq, D] over the pools."""
+    NB, bs, Hkv, D = k_cache.shape
+    B, Hq, Dq = q.shape
+    if Dq != D or tuple(out.shape) != (B, Hq, D) or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("shape mismatch")
+    dt = _dtype(q)
+    if out.dtype != q.dtype or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise TypeError("q, out and the pools must share a dtype")
+    maxb = block_tables.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("pa_decode", load().pa_decode(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _i32(block_tables, "block_tables"), maxb,
+        _i32(context_lens, "context_lens"), B, Hq, Hkv, D, bs, NB, float(scale), dt,
+        _ptr(workspace), ws_bytes, _i32(err, "err"), _stream(stream)))
+
+
+def pa_prefill_varlen(out, q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
+                      max_seqlen_q: int, max_seqlen_k: int, block_tables=None, *, Hkv: int,
+                      scale: float, causal: bool = True, err=None, stream=None) -> None:
+    """Varlen (causal) prefill: out [Tq, Hq, D]. Keys come from the pools through block_tables,
+    or from the packed k, v when block_tables is None."""
+    Tq, Hq, D = q.shape
+    if tuple(out.shape) != (Tq, Hq, D):
+        raise ValueError("out must match q")
+    S = cu_seqlens_q.shape[0] - 1
+    if cu_seqlens_k.shape[0] != S + 1:
+        raise ValueError("cu_seqlens_k must have S+1 entries")
+    dt = _dtype(q)
+    if block_tables is not None:
+        NB, bs, Hkv_c, Dc = k_cache.shape
+        if Hkv_c != Hkv or Dc != D or block_tables.shape[0] != S:
+            raise ValueError("pool / table shape mismatch")
+        maxb = block_tables.shape[1]
+    else:
+        NB, bs, maxb = 0, 1, 0
+        if k.shape[1:] != (Hkv, D) or v.shape != k.shape:
+            raise ValueError("packed k, v must be [Tk, Hkv, D]")
+    for t in (out, k, v, k_cache, v_cache):
+        if t is not None and t.dtype != q.dtype:
+            raise TypeError("all attention tensors must share a dtype")
+    _check("pa_prefill_varlen", load().pa_prefill_varlen(
+        _ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
+        _i32(cu_seqlens_q, "cu_seqlens_q"), _i32(cu_seqlens_k, "cu_seqlens_k"), S,
+        int(max_seqlen_q), int(max_seqlen_k), _i32(block_tables, "block_tables"), maxb, Hq, Hkv, D,
+        bs, NB, float(scale), int(bool(causal)), dt, _i32(err, "err"), _stream(stream)))

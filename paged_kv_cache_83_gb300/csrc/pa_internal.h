@@ -1,0 +1,65 @@
+// pa_internal.h: argument bundles and launchers behind the C ABI (include/pa.h).
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+int device_sm_count();  // SMs of the current device (cached per device)
+
+// ------------------------------------------------------------------------------------------
+struct StoreArgs {
+    const void *k, *v;
+    void *k_cache, *v_cache;
+    const int32_t *slot_mapping;
+    int T, num_blocks, block_size, Hkv, D;
+    int32_t *err;
+};
+cudaError_t launch_store_kv(const StoreArgs &a, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+// Split-K decode. A sequence's context is cut into chunks of `chunk` positions; CTA
+// (split, kv head, sequence) handles one chunk for the whole GQA group of that kv head.
+struct DecodePlan {
+    int chunk;       // positions per split (a multiple of the 64-position tile)
+    int max_splits;  // ceil(max context / chunk)
+    int tbl_cap;     // block-table entries one chunk can span
+    size_t ws_bytes; // scratch for partial results (0 when max_splits == 1)
+};
+DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int block_size);
+
+struct DecodeArgs {
+    void *out;
+    const void *q, *k_cache, *v_cache;
+    const int32_t *block_tables, *context_lens;
+    int B, Hq, Hkv, D, max_blocks, block_size, num_blocks;
+    float scale;
+    pa_dtype dtype;
+    void *workspace;
+    int32_t *err;
+};
+cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+struct PrefillArgs {
+    void *out;
+    const void *q, *k, *v, *k_cache, *v_cache;
+    const int32_t *cu_q, *cu_k, *block_tables;
+    int S, max_seqlen_q, max_blocks, Hq, Hkv, D, block_size, num_blocks, causal;
+    float scale;
+    pa_dtype dtype;
+    int32_t *err;
+};
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
+inline int log2_if_pow2(int x) {
+    if (x <= 0 || (x & (x - 1))) return -1;
+    int s = 0;
+    while ((1 << s) < x) ++s;
+    return s;
+}
+
+}  // namespace pa

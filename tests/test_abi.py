@@ -1,0 +1,115 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point that include/pa.h
+declares, and its host-side argument checks return the documented status codes before any
+CUDA work (no kernel is launched by these calls)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+import paged_kv_cache_83_gb300 as pa
+from paged_kv_cache_83_gb300 import binding
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+def declared_functions():
+    text = (ROOT / "include" / "pa.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not binding.LIB_PATH.exists():
+        from paged_kv_cache_83_gb300 import build
+        build.build()
+    return pa.load()
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("pa_store_kv", "pa_decode", "pa_prefill_varlen", "pa_decode_workspace_size",
+              "pa_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+    assert set(binding.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.pa_status_string(code)
+    assert lib.pa_status_string(0) == b"ok"
+
+
+# A non-null, 16-byte aligned dummy address. Every call below that passes FAKE is built to fail a
+# host-side check (or to be an empty no-op), so no kernel ever launches on it.
+FAKE = 1 << 20
+
+
+def test_store_kv_host_checks(lib):
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE]
+    assert lib.pa_store_kv(*args, 4, 8, 16, 2, 64, 7, None, None) == 3        # dtype
+    assert lib.pa_store_kv(*args, -1, 8, 16, 2, 64, 0, None, None) == 2       # T < 0
+    assert lib.pa_store_kv(*args, 4, 8, 0, 2, 64, 0, None, None) == 2         # block_size 0
+    assert lib.pa_store_kv(*args, 4, 8, 16, 2, 60, 0, None, None) == 4        # D % 8
+    assert lib.pa_store_kv(*args, 0, 8, 16, 2, 64, 0, None, None) == 0        # empty: no-op
+    assert lib.pa_store_kv(None, FAKE, FAKE, FAKE, FAKE, 4, 8, 16, 2, 64, 0, None, None) == 1
+    assert lib.pa_store_kv(FAKE + 2, FAKE, FAKE, FAKE, FAKE, 4, 8, 16, 2, 64, 0, None, None) == 4
+
+
+def _decode(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, maxb=4, cl=FAKE, B=2, Hq=4, Hkv=2, D=64,
+             bs=16, nb=8, scale=0.125, dt=0, ws=None, wsb=0, err=None, stream=None)
+    a.update(kw)
+    return lib.pa_decode(*a.values())
+
+
+def test_decode_host_checks(lib):
+    assert _decode(lib, dt=2) == 3
+    assert _decode(lib, Hq=5) == 2          # Hq % Hkv
+    assert _decode(lib, Hq=18) == 4         # group of 9
+    assert _decode(lib, D=96) == 4
+    assert _decode(lib, bs=0) == 2
+    assert _decode(lib, B=0) == 0           # empty batch: no-op
+    assert _decode(lib, q=None) == 1
+    assert _decode(lib, bt=None) == 1
+    assert _decode(lib, out=FAKE + 8) == 4  # misaligned
+    need = lib.pa_decode_workspace_size(2, 4, 2, 64, 4, 16)
+    if need:
+        assert _decode(lib, ws=None, wsb=0) == 5
+        assert _decode(lib, ws=FAKE, wsb=need - 1) == 5
+
+
+def _prefill(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, S=2, mq=8, mk=8,
+             bt=FAKE, maxb=2, Hq=4, Hkv=2, D=128, bs=16, nb=8, scale=0.1, causal=1, dt=1, err=None,
+             stream=None)
+    a.update(kw)
+    return lib.pa_prefill_varlen(*a.values())
+
+
+def test_prefill_host_checks(lib):
+    assert _prefill(lib, dt=9) == 3
+    assert _prefill(lib, S=-1) == 2
+    assert _prefill(lib, causal=2) == 2
+    assert _prefill(lib, D=80) == 4
+    assert _prefill(lib, S=0) == 0
+    assert _prefill(lib, mq=0) == 0
+    assert _prefill(lib, kc=None) == 1               # table given, pool missing
+    assert _prefill(lib, bt=None, k=None) == 1       # packed keys missing
+    assert _prefill(lib, cq=None) == 1
+    assert _prefill(lib, bs=0) == 2
+
+
+def test_workspace_size_rules(lib):
+    assert lib.pa_decode_workspace_size(0, 4, 2, 64, 4, 16) == 0
+    assert lib.pa_decode_workspace_size(2, 4, 3, 64, 4, 16) == 0      # invalid heads
+    small = lib.pa_decode_workspace_size(2, 4, 2, 64, 4, 16)
+    big = lib.pa_decode_workspace_size(2, 4, 2, 64, 400, 16)
+    assert big >= small

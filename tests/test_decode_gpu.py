@@ -1,0 +1,177 @@
+"""pa_decode on the GPU against the fp64 oracle (store first, as one decode layer step).
+
+Small cases are compared element by element; the full-size workloads (the launch
+configuration the bench times) on sampled sequences the oracle computes one by one, always
+including the shortest and longest contexts. Tolerance: max-abs 2e-3 (fp16), 1e-2 (bf16).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_83_gb300 as pa
+import workloads as W
+from tests.gpu_util import TOL, DecodeRun, bits, err_buf, f64, i32, max_abs, to_dev, workspace
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.get()
+
+
+def _reference(orc, c, kc_bits, vc_bits, rows=None):
+    if rows is None:
+        return orc.decode(c.q, kc_bits, vc_bits, c.block_tables, c.context_lens, scale=c.scale,
+                          dtype=c.dtype)
+    return orc.decode(c.q[rows], kc_bits, vc_bits, c.block_tables[rows], c.context_lens[rows],
+                      scale=c.scale, dtype=c.dtype)
+
+
+def _check_full(orc, c):
+    run = DecodeRun(c)
+    out = f64(run.step())
+    kc_ref, vc_ref = orc.store_kv(c.k_new, c.v_new, c.k_cache, c.v_cache, c.slot_mapping)
+    assert np.array_equal(bits(run.kc), kc_ref) and np.array_equal(bits(run.vc), vc_ref)
+    ref = _reference(orc, c, kc_ref, vc_ref)
+    e = max_abs(out, ref)
+    assert e <= TOL[c.dtype], e
+    assert int(run.err.item()) == 0
+    return e
+
+
+def test_tiny_config(orc):
+    _check_full(orc, W.make("tiny"))
+
+
+@pytest.mark.parametrize("name,n", [("qwen25_05b_decode", 6), ("qwen3_06b_decode", 5),
+                                    ("longtail_decode", 7)])
+def test_shrunken_configs_elementwise(orc, name, n):
+    _check_full(orc, W.make(name, n=n))
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("D,dt", [(64, "f16"), (128, "bf16")])
+def test_group_sizes(orc, G, D, dt):
+    Hkv = 2
+    lens = [1, 63, 64, 65, 200, 700]
+    c = W.decode_case(B=len(lens), Hq=G * Hkv, Hkv=Hkv, D=D, block_size=16, dtype=dt,
+                      context_lens=lens, seed=G)
+    _check_full(orc, c)
+
+
+@pytest.mark.parametrize("bs", [1, 3, 4, 16, 64, 256])
+def test_block_sizes(orc, bs):
+    lens = [1, 2, bs, bs + 1, 129, 511, 1000]
+    c = W.decode_case(B=len(lens), Hq=8, Hkv=4, D=128, block_size=bs, dtype="bf16",
+                      context_lens=lens, seed=bs, placement="interleaved")
+    _check_full(orc, c)
+
+
+def test_zero_context_and_padding_rows(orc):
+    lens = [0, 5, 0, 300]
+    c = W.decode_case(B=4, Hq=4, Hkv=2, D=64, block_size=16, dtype="f16", context_lens=lens,
+                      seed=3, pad_slots=0)
+    run = DecodeRun(c)
+    out = f64(run.step())
+    assert not out[0].any() and not out[2].any()
+    kc_ref, vc_ref = orc.store_kv(c.k_new, c.v_new, c.k_cache, c.v_cache, c.slot_mapping)
+    assert max_abs(out, _reference(orc, c, kc_ref, vc_ref)) <= TOL["f16"]
+
+
+def test_single_token_returns_its_value(orc):
+    c = W.decode_case(B=3, Hq=6, Hkv=3, D=128, block_size=256, dtype="bf16", context_lens=[1, 1, 1],
+                      seed=4)
+    out = f64(DecodeRun(c).step())
+    v = (c.v_new.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for h in range(6):
+        assert np.array_equal(out[:, h], v[:, h // 2])
+
+
+def test_max_context(orc):
+    # one sequence at the longest context the long-tail workload allows (16384)
+    c = W.decode_case(B=2, Hq=16, Hkv=8, D=128, block_size=256, dtype="bf16",
+                      context_lens=[16384, 9000], seed=5, placement="interleaved")
+    _check_full(orc, c)
+
+
+def test_batch_equals_alone():
+    c = W.make("qwen3_06b_decode", n=6)
+    run = DecodeRun(c)
+    batched = run.step().clone()
+    for i in (0, 3, 5):
+        out = torch.empty(1, c.Hq, c.D, dtype=run.q.dtype, device="cuda")
+        pa.pa_decode(out, run.q[i:i + 1].contiguous(), run.kc, run.vc, run.bt[i:i + 1].contiguous(),
+                     run.cl[i:i + 1].contiguous(), c.scale,
+                     workspace=workspace(1, c.Hq, c.Hkv, c.D, c.max_blocks_per_seq, c.block_size))
+        torch.cuda.synchronize()
+        # the split plan depends on the batch size, so only the summation order may differ
+        assert max_abs(f64(out[0]), f64(batched[i])) <= TOL[c.dtype]
+
+
+def test_invalid_table_entry_is_flagged_and_masked(orc):
+    c = W.decode_case(B=2, Hq=4, Hkv=2, D=64, block_size=16, dtype="f16", context_lens=[40, 40],
+                      seed=6)
+    bt = c.block_tables.copy()
+    bt[1, 1] = c.num_blocks + 7          # positions 16..31 of sequence 1 point outside the pool
+    run = DecodeRun(c)
+    run.bt = i32(bt)
+    out = f64(run.step())
+    assert int(run.err.item()) & pa.PA_DEVERR_TABLE
+    kc_ref, vc_ref = orc.store_kv(c.k_new, c.v_new, c.k_cache, c.v_cache, c.slot_mapping)
+    ref0 = orc.decode(c.q[:1], kc_ref, vc_ref, c.block_tables[:1], c.context_lens[:1],
+                      scale=c.scale, dtype=c.dtype)
+    assert max_abs(out[:1], ref0) <= TOL["f16"]      # the healthy sequence is untouched
+    assert np.isfinite(out[1]).all()
+
+
+def test_context_longer_than_table_is_flagged_and_zeroed():
+    c = W.decode_case(B=2, Hq=4, Hkv=2, D=64, block_size=16, dtype="f16", context_lens=[20, 20],
+                      seed=7)
+    run = DecodeRun(c)
+    run.cl = i32(np.array([20, c.max_blocks_per_seq * 16 + 1]))
+    out = f64(run.step())
+    assert int(run.err.item()) & pa.PA_DEVERR_LENGTH
+    assert not out[1].any()
+
+
+def test_workspace_too_small_is_refused():
+    c = W.make("qwen25_05b_decode", n=4)
+    run = DecodeRun(c)
+    need = pa.pa_decode_workspace_size(c.B, c.Hq, c.Hkv, c.D, c.max_blocks_per_seq, c.block_size)
+    assert need > 0
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pa.PagedAttnError) as ei:
+        pa.pa_decode(run.out, run.q, run.kc, run.vc, run.bt, run.cl, c.scale, workspace=small)
+    assert ei.value.status == 5
+
+
+def test_empty_batch_is_noop():
+    q = torch.empty(0, 4, 64, dtype=torch.float16, device="cuda")
+    kc = torch.zeros(2, 16, 2, 64, dtype=torch.float16, device="cuda")
+    pa.pa_decode(q, q, kc, kc, torch.empty(0, 1, dtype=torch.int32, device="cuda"),
+                 torch.empty(0, dtype=torch.int32, device="cuda"), 0.125)
+    torch.cuda.synchronize()
+
+
+def _sampled_full_size(orc, name, nsample=12):
+    c = W.make(name)
+    run = DecodeRun(c)
+    out = f64(run.step())
+    assert int(run.err.item()) == 0
+    assert np.isfinite(out).all()
+    rng = np.random.default_rng(17)
+    rows = sorted(set([int(np.argmin(c.context_lens)), int(np.argmax(c.context_lens))] +
+                      list(rng.choice(c.B, size=nsample, replace=False))))
+    # the oracle's own scatter gives the pools it attends over; the GPU's pools must equal them
+    kc_ref, vc_ref = orc.store_kv(c.k_new, c.v_new, c.k_cache, c.v_cache, c.slot_mapping)
+    assert np.array_equal(bits(run.kc), kc_ref) and np.array_equal(bits(run.vc), vc_ref)
+    ref = _reference(orc, c, kc_ref, vc_ref, rows)
+    e = max_abs(out[rows], ref)
+    assert e <= TOL[c.dtype], e
+
+
+@pytest.mark.parametrize("name", ["qwen25_05b_decode", "qwen3_06b_decode", "longtail_decode"])
+def test_full_size_sampled(orc, name):
+    _sampled_full_size(orc, name)
