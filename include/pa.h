@@ -164,6 +164,35 @@ pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void 
                             int num_blocks, float scale, int causal, pa_dtype dtype,
                             int32_t *err, cudaStream_t stream);
 
+/*
+ * pa_decode_noalloc: pa_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call; it exists for users of the library that cannot
+ * provide pa_decode's workspace: a host framework that owns every device allocation and gives
+ * its plugins none, a process whose device memory is already fully reserved by another
+ * allocator, or a step loop that cannot afford cudaMalloc's implicit device synchronisation.
+ *
+ * It computes exactly what pa_decode computes, with the same arguments minus the workspace. Its
+ * split-K scratch is one file-scope device array of PA_DECODE_NOALLOC_SCRATCH_BYTES (32 MiB),
+ * which every GPU that loads this library holds until the process exits. The call itself
+ * allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ * - Limit: sizes whose pa_decode_workspace_size() exceeds PA_DECODE_NOALLOC_SCRATCH_BYTES are
+ *   rejected with PA_ERR_WORKSPACE before anything is launched (use pa_decode for them).
+ * - Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ *   capture. A failed lookup returns PA_ERR_CUDA.
+ * - Sharing: every call on a device uses the same array and leaves the last call's partial
+ *   results in it. Nothing in it needs to start at zero, but calls that overlap on the GPU
+ *   (on different streams, or from different host threads) race on it: serialise them.
+ */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
+pa_status pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, int B, int Hq, int Hkv, int D,
+                            int block_size, int num_blocks, float scale, pa_dtype dtype,
+                            int32_t *err, cudaStream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char *pa_status_string(pa_status status);
 

@@ -18,7 +18,8 @@ LIB_PATH = PKG / "_build" / "libpagedattn.so"
 PA_F16, PA_BF16 = 0, 1
 PA_DEVERR_SLOT, PA_DEVERR_TABLE, PA_DEVERR_LENGTH = 1, 2, 4
 EXPORTS = ("pa_store_kv", "pa_decode_workspace_size", "pa_decode", "pa_prefill_varlen",
-           "pa_status_string")
+           "pa_decode_noalloc", "pa_status_string")
+PA_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _lib = None
 
@@ -48,6 +49,8 @@ def load(path: Path | str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_prefill_varlen.argtypes = [P, P, P, P, P, P, P, P, I, I, I, P, I, I, I, I, I, I, F, I,
                                       I, P, P]
     lib.pa_prefill_varlen.restype = I
+    lib.pa_decode_noalloc.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, P, P]
+    lib.pa_decode_noalloc.restype = I
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -131,6 +134,25 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _i32(block_tables, "block_tables"), maxb,
         _i32(context_lens, "context_lens"), B, Hq, Hkv, D, bs, NB, float(scale), dt,
         _ptr(workspace), ws_bytes, _i32(err, "err"), _stream(stream)))
+
+
+def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                      err=None, stream=None) -> None:
+    """pa_decode without a workspace argument: for callers that cannot allocate device memory.
+    Its scratch is the library's fixed device array (PA_DECODE_NOALLOC_SCRATCH_BYTES); sizes
+    that need more raise PagedAttnError with status 5. Calls that overlap on the GPU race on
+    that array."""
+    NB, bs, Hkv, D = k_cache.shape
+    B, Hq, Dq = q.shape
+    if Dq != D or tuple(out.shape) != (B, Hq, D) or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("shape mismatch")
+    dt = _dtype(q)
+    if out.dtype != q.dtype or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise TypeError("q, out and the pools must share a dtype")
+    _check("pa_decode_noalloc", load().pa_decode_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _i32(block_tables, "block_tables"),
+        block_tables.shape[1], _i32(context_lens, "context_lens"), B, Hq, Hkv, D, bs, NB,
+        float(scale), dt, _i32(err, "err"), _stream(stream)))
 
 
 def pa_prefill_varlen(out, q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
