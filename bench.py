@@ -366,7 +366,7 @@ def run_gpu(args, ws_, rank, local):
     rows["store_kv_decode"] = {"kernel": "store_kv_kernel", "ms": st_mean,
                                "GB_per_s": st_bytes / (st_mean * 1e-3) / 1e9,
                                "bytes": st_bytes, "note": "256 new rows: launch-latency bound"}
-    rows["decode"] = {"kernel": "decode_split_kernel + decode_merge_kernel", "ms": dec_mean,
+    rows["decode"] = {"kernel": "decode_kernel + decode_merge_kernel", "ms": dec_mean,
                       "GB_per_s": achieved, "frac_of_hbm": achieved / hbm}
 
     cpu = None
@@ -395,7 +395,7 @@ def run_gpu(args, ws_, rank, local):
         "decode_steps_per_sec_per_layer": 1e3 / ms_step,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
-                     "kernel": "pa_decode: decode_split_kernel + decode_merge_kernel",
+                     "kernel": "pa_decode: decode_kernel + decode_merge_kernel",
                      "peak_source": f"{pk_kind} hbm_gbs"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,

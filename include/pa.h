@@ -63,6 +63,9 @@ typedef enum { PA_F16 = 0, PA_BF16 = 1 } pa_dtype;
 #define PA_DEVERR_LENGTH 4 /* a context length or cu_seqlens span outside its contract
                               (negative, longer than the block table covers, k_len < q_len,
                               q_len > max_seqlen_q): the sequence's output rows are zero */
+#define PA_DEVERR_TIMEOUT 8 /* an internal wait (on an asynchronous copy or on another warp)
+                               gave up after about half a second: the kernel stopped early and
+                               its outputs are incomplete */
 
 /*
  * pa_store_kv: scatter this step's new K and V rows into the pools.
@@ -88,8 +91,10 @@ pa_status pa_store_kv(const void *k, const void *v, void *k_cache, void *v_cache
 
 /*
  * pa_decode_workspace_size: bytes of scratch pa_decode needs for these sizes on the current
- * device (split-K partial results: per (sequence, query head, split) D fp32 values plus the
- * running max and sum). 0 means no scratch is needed. Never fails; returns 0 for sizes that
+ * device: for each SM, two partial results (G query heads x (D + 2) fp32: output, running max,
+ * sum) of the at most two context pieces it shares with a neighbour, plus a 48-byte record. It
+ * depends only on the group size G = Hq / Hkv, D and the SM count (about 1.3 MB at most on a
+ * GB300), not on the batch or the context lengths. Never fails; returns 0 for sizes that
  * pa_decode would reject.
  */
 size_t pa_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_blocks_per_seq,
@@ -173,7 +178,7 @@ pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void 
  * allocator, or a step loop that cannot afford cudaMalloc's implicit device synchronisation.
  *
  * It computes exactly what pa_decode computes, with the same arguments minus the workspace. Its
- * split-K scratch is one file-scope device array of PA_DECODE_NOALLOC_SCRATCH_BYTES (32 MiB),
+ * split-K scratch is one file-scope device array of PA_DECODE_NOALLOC_SCRATCH_BYTES (1 MiB),
  * which every GPU that loads this library holds until the process exits. The call itself
  * allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  *
@@ -186,7 +191,7 @@ pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void 
  *   results in it. Nothing in it needs to start at zero, but calls that overlap on the GPU
  *   (on different streams, or from different host threads) race on it: serialise them.
  */
-#define PA_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES (1u << 20)
 pa_status pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *block_tables, int max_blocks_per_seq,
                             const int32_t *context_lens, int B, int Hq, int Hkv, int D,

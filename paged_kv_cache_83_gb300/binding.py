@@ -19,7 +19,7 @@ PA_F16, PA_BF16 = 0, 1
 PA_DEVERR_SLOT, PA_DEVERR_TABLE, PA_DEVERR_LENGTH = 1, 2, 4
 EXPORTS = ("pa_store_kv", "pa_decode_workspace_size", "pa_decode", "pa_prefill_varlen",
            "pa_decode_noalloc", "pa_status_string")
-PA_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
+PA_DECODE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 _lib = None
 

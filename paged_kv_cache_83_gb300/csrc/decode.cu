@@ -1,24 +1,34 @@
-// decode.cu: paged grouped-query decode attention (pa_decode): split-K kernel + merge kernel.
+// decode.cu: paged grouped-query decode attention (pa_decode).
 //
 // Source: "nano-vLLM Part 4", section 3 (decode: one already-sampled token per sequence,
 // attention over its cached history through a block table); "mini-vLLM" (one token per
 // sequence attending to that sequence's cached keys and values, grouped-query attention).
 //
-// Design (GB300): decode reads every cached K/V row once and does ~G multiply-adds per byte,
-// far below the HBM ridge, so the kernel is built to keep HBM busy, not to reach tensor cores.
-//  * Work item = (sequence, kv head, chunk of `chunk` positions). One CTA computes the whole
-//    GQA group (G query heads) of its kv head, so each K/V byte is read from HBM once.
-//  * 64-position tiles of K and V are staged into shared memory with 16-byte cp.async copies,
-//    STAGES deep; each copy's address goes through the block table (kept in shared memory for
-//    the chunk). Rows past the context or in an invalid block are zero-filled and masked.
-//  * QK: LPP lanes share one position, each holding E query elements per head in registers
-//    (pre-multiplied by scale*log2 e); partial dots meet in a butterfly of shuffles. The K tile
-//    is stored with a 16-byte-chunk XOR swizzle so these reads are free of bank conflicts.
-//  * Softmax is online per warp in base 2; PV: each lane owns 8 output columns of a row
-//    group and accumulates p * V from the unswizzled V tile.
-//  * At the end the 4 warps' (max, sum, O) are combined in shared memory. A single-split
-//    sequence writes its output directly; otherwise the normalised partial and its (max, sum)
-//    go to the workspace and decode_merge_kernel combines the splits.
+// Decode reads every cached K/V row once and does ~G multiply-adds per byte, far below the HBM
+// ridge, so the kernel is organised to keep HBM streaming, not to reach the tensor cores.
+//
+// Work: the flattened space of 128-position tiles over (sequence b, kv head g, tile t), ordered
+// b, then g, then t, is cut into one equal contiguous range per CTA (one persistent CTA per SM),
+// so every SM streams the same number of bytes and no CTA is a straggler. A CTA's range covers
+// whole (b, g) pairs plus at most a partial pair at each end ("segments").
+//
+// CTA = 1 producer warp + 8 consumer warps.
+//  * Producer: walks the range; for each tile it looks the rows' physical blocks up in the block
+//    table and issues TMA loads of the K and V tile rows (one box per run of `box_rows` rows that
+//    share a block) into a ring of shared-memory stages, plus a bulk copy of the G query rows at
+//    the start of each segment. full/empty mbarriers hand stages to and from the consumers; the
+//    ring (2-6 stages of 32-64 KB) keeps up to ~130 KB per SM in flight across pair boundaries.
+//  * Consumers: warp w owns rows 16w..16w+15 of every 128-row tile. QK: LPP lanes per row, each holding E
+//    query elements per head (scaled by scale*log2 e) and multiplying with packed fp32 pairs
+//    (two independent passes of 8 rows);
+//    the chunk each lane reads depends on the lane so that rows sharing a bank phase hit
+//    disjoint banks of the unswizzled tile. Online softmax in base 2 per warp; PV with each lane
+//    owning 8 output columns. At a segment's end the 8 warps' (max, sum, O) are combined: a
+//    segment covering its whole pair writes the output; a partial segment writes (O/sum, max,
+//    sum) to one of the CTA's two workspace slots, and decode_merge_kernel combines the pieces.
+//  * Every wait is bounded (PA_DEVERR_TIMEOUT); the producer drains its copies before exiting.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
 
 #include "pa_internal.h"
@@ -27,378 +37,739 @@ namespace pa {
 
 namespace {
 
-constexpr int kTN = 64;             // positions per tile
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kWPos = kTN / kWarps;  // positions per warp per tile
+constexpr int kTN = 64;                  // positions per tile
+constexpr int kConsumers = 8;            // consumer warps
+constexpr int kWPos = kTN / kConsumers;  // rows per consumer warp per tile
+constexpr int kThreads = 32 * (1 + kConsumers);
+constexpr int kConsThreads = 32 * kConsumers;
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kSmemPerSm = 227 * 1024;
+// persistent CTAs per SM: two (two TMA streams, 16 consumer warps) when the group is small
+// enough for the halved register file, else one
+template <int G>
+constexpr int ctas_per_sm() { return G <= 3 ? 2 : 1; }
 
-template <int D, int G>
-struct Shape {
-    static constexpr int NCH = D / 8;  // 16-byte chunks per row
-    static constexpr int E_RAW = G == 1 ? 64 : G == 2 ? 32 : G <= 4 ? 16 : 8;
-    static constexpr int E = E_RAW < D / 2 ? E_RAW : D / 2;  // QK elements per lane
-    static constexpr int LPP = D / E;                         // lanes per position in QK
-    static constexpr int PPP = 32 / LPP;                      // positions per QK pass
-    static constexpr int PASSES = kWPos / PPP;
-    static constexpr int CPL = E / 8;                         // 16-byte chunks per lane in QK
-    static constexpr int LPR = NCH;                           // PV lanes per row (8 columns each)
-    static constexpr int RPI = 32 / LPR;                      // PV rows per warp instruction
-    static constexpr int STAGES = D == 128 ? 3 : 4;
-    static constexpr int TILE_BYTES = kTN * D * 2;
-    static constexpr int TILES_BYTES = 2 * STAGES * TILE_BYTES;
-    static constexpr int LOADS = kTN * NCH / kThreads;         // 16-byte copies per thread per tile
-    // XOR applied to the chunk index of K row `row`: positions that share a bank phase in
-    // QK get disjoint bank groups
-    static __device__ __forceinline__ int swz(int row) {
-        return LPP < 8 ? (row % (8 / LPP)) * LPP : 0;
-    }
-    static_assert(PASSES >= 1 && PPP * PASSES == kWPos, "QK mapping");
-    static_assert(LOADS * kThreads == kTN * NCH, "loader mapping");
+// flags of one tile
+constexpr int kFirst = 1;  // first tile of a segment: reset the state, read q
+constexpr int kLast = 2;   // last tile of a segment: combine the warps and write
+constexpr int kWhole = 4;  // the segment is its pair's whole context: write the output
+constexpr int kSlot1 = 8;  // partial segment that is not the CTA's first: workspace slot 1
+
+struct TileMeta {
+    int b, g, flags, all_valid;  // all_valid: every one of the 128 rows is a context position
+    unsigned long long valid[2];  // bit r of the 128-bit mask: tile row r is a context position
+};
+
+// What the merge kernel needs to know about one CTA.
+struct SegRecord {
+    long long lo, hi;        // the CTA's tile range
+    long long pair_start;    // global index of the first tile of the CTA's first pair
+    long long total;         // tiles in the whole launch
+    int b, g, ntiles, pad;   // that pair and its tile count; b < 0: empty range
 };
 
 struct DecodeParams {
-    const void *q, *k_cache, *v_cache;
+    CUtensorMap tmap_k, tmap_v;  // [slots, Hkv, D] views of the pools, box [box_rows, 1, D]
+    const void *q;
     const int32_t *block_tables, *context_lens;
     void *out;
-    float *ws_o;   // [B, Hq, max_splits, D]
-    float *ws_ml;  // [B, Hq, max_splits, 2]  (max in log2 units, sum)
+    float *part;     // [P][2][G][D + 2]: normalised O, max (log2 units), sum
+    SegRecord *rec;  // [P]
     int32_t *err;
-    int B, Hq, Hkv, max_blocks, num_blocks, chunk, max_splits, tbl_cap;
+    int B, Hq, Hkv, max_blocks, num_blocks, box_rows, stages;
     BlockGeom geom;
     float scale_log2;
 };
 
 template <int D, int G>
-constexpr int smem_bytes_for(int tbl_cap) {
-    return Shape<D, G>::TILES_BYTES + tbl_cap * 4 + 2 * kWarps * G * kWPos * 4;
+struct Shape {
+    static constexpr int NCH = D / 8;  // 16-byte chunks per row
+    static constexpr int CPS = ctas_per_sm<G>();
+    // QK elements per lane: keeps the query registers (G * E) at 32 with two CTAs per SM,
+    // at 64 with one
+    static constexpr int E_RAW = CPS == 2 ? (G == 1 ? 32 : G == 2 ? 16 : 8) : (G <= 4 ? 16 : 8);
+    static constexpr int E = E_RAW < D / 4 ? E_RAW : D / 4;  // QK elements per lane
+    static constexpr int LPP = D / E;                         // lanes per row in QK
+    static constexpr int PPP = 32 / LPP;                      // rows per QK pass
+    static constexpr int PASSES = kWPos / PPP;
+    static constexpr int CPL = E / 8;                         // chunks per lane in QK
+    static constexpr int CPV = G >= 6 ? 4 : 8;                // PV output columns per lane
+    static constexpr int NPV = CPV / 2;                       // ... as fp32 pairs
+    static constexpr int LPR = D / CPV;                       // PV lanes per row
+    static constexpr int RPI = 32 / LPR;                      // PV rows per instruction
+    static constexpr int PV_IT = kWPos / RPI;
+    static constexpr int HPR = 32 / kWPos;                    // softmax heads per round
+    static constexpr int ROUNDS = (G + HPR - 1) / HPR;
+    static constexpr int TILE_BYTES = kTN * D * 2;
+    static constexpr int Q_BYTES = G * D * 2;
+    static constexpr int STAGE_BYTES = (2 * TILE_BYTES + Q_BYTES + 1023) / 1024 * 1024;
+    static constexpr int RED_BYTES = kConsumers * G * (D + 2) * 4;
+    static constexpr int SCRATCH_BYTES = 2 * kConsumers * G * kWPos * 4 + kConsumers * G * 4;
+    static_assert(PASSES >= 1 && PPP * PASSES == kWPos, "QK mapping");
+    static_assert(RPI * PV_IT == kWPos, "PV mapping");
+    // chunk that lane (row u of a pass, part r) reads at step c. With 4 lanes per row two rows
+    // share an 8-lane bank phase: they take opposite 64-byte halves of each 128-byte group.
+    static __device__ __forceinline__ int chunk(int c, int r, int u) {
+        if (LPP == 4) return 8 * (c >> 1) + 4 * ((c & 1) ^ (u & 1)) + r;
+        return c * LPP + r;
+    }
+};
+
+template <int D, int G>
+constexpr int fixed_smem() {
+    // + metas, barriers, scan scratch (1 KB) and the slack that aligns the ring (1 KB)
+    return Shape<D, G>::RED_BYTES + Shape<D, G>::SCRATCH_BYTES + 2048;
+}
+
+// All 32 lanes wait for the phase, then the warp reconverges; false (for every lane) if the wait
+// ran out or the CTA is aborting.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+    const bool ok = mbar_wait(bar, parity) && !*abort_flag;
+    const bool all = __all_sync(kFull, ok);
+    __syncwarp();
+    return all;
+}
+
+// validity of consumer warp cw's kWPos rows, as the low bits of a word
+__device__ __forceinline__ unsigned warp_rows_valid(const TileMeta &m, int cw) {
+    const int first = cw * kWPos;
+    const unsigned long long w = m.valid[first >> 6];
+    return static_cast<unsigned>(w >> (first & 63)) & ((1u << kWPos) - 1u);
+}
+
+__device__ __forceinline__ int ntiles_of(const DecodeParams &p, int b, long long cap) {
+    const int n = p.context_lens[b];
+    if (n <= 0 || n > cap) return 0;
+    return (n + kTN - 1) / kTN;
+}
+
+// block-wide sum over all kThreads threads; `red` holds kThreads / 32 longs
+__device__ long long block_sum(long long v, long long *red) {
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) red[w] = v;
+    __syncthreads();
+    long long t = 0;
+    for (int i = 0; i < kThreads / 32; ++i) t += red[i];
+    __syncthreads();
+    return t;
 }
 
 template <int D, int G, class E>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(const __grid_constant__ DecodeParams p) {
     using S = Shape<D, G>;
     using T = typename E::T;
-    extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char *ks = smem;
-    unsigned char *vs = smem + S::STAGES * S::TILE_BYTES;
-    int *tbl = reinterpret_cast<int *>(smem + S::TILES_BYTES);
-    float *sbuf = reinterpret_cast<float *>(tbl + p.tbl_cap);  // [warps][G][16] raw scores
-    float *pbuf = sbuf + kWarps * G * kWPos;                    // [warps][G][16] probabilities
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // stages start on a 1024-byte boundary (the launch adds 1 KB of slack for this)
+    unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const int NS = p.stages;
+    unsigned char *ring = smem;
+    float *red = reinterpret_cast<float *>(smem + NS * S::STAGE_BYTES);  // [8][G][D+2]
+    float *sbuf = red + kConsumers * G * (D + 2);                        // [8][G][16] scores
+    float *pbuf = sbuf + kConsumers * G * kWPos;                         // [8][G][16] probs
+    float *abuf = pbuf + kConsumers * G * kWPos;                         // [8][G] rescale
+    TileMeta *metas = reinterpret_cast<TileMeta *>(abuf + kConsumers * G);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(metas + NS);  // full[NS], empty[NS], cons[2]
+    long long *scan = reinterpret_cast<long long *>(bars + 2 * NS + 2);  // 16 longs + start
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(scan + 20);
 
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hq0 = g * G;
-
-    int n = p.context_lens[b];
+    const int P = gridDim.x, cta = blockIdx.x;
     const long long cap = static_cast<long long>(p.max_blocks) * p.geom.block_size;
-    if (n < 0 || n > cap) {
-        if (split == 0 && tid == 0) raise_err(p.err, PA_DEVERR_LENGTH);
-        n = 0;
+    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + NS),
+                   cons0 = smem_addr(bars + 2 * NS);
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kConsumers);
+        }
+        mbar_init(cons0, kConsumers);
+        mbar_init(cons0 + 8, kConsumers);
+        *abort_flag = 0;
+        fence_mbar_init();
     }
-    if (n == 0) {  // no keys: zero output, written by the first split only
-        if (split == 0) {
-            T *o = static_cast<T *>(p.out) + (static_cast<size_t>(b) * p.Hq + hq0) * D;
-            for (int i = tid; i < G * D; i += kThreads) o[i] = T(0.f);
+
+    // ---- pass 1: tiles per sequence, the total, zero rows of empty sequences ----
+    long long mine = 0;
+    for (int b = tid; b < p.B; b += kThreads) {
+        const int n = p.context_lens[b];
+        if (n < 0 || n > cap) {
+            if (b % P == cta) raise_err(p.err, PA_DEVERR_LENGTH);
+        }
+        const int nt = ntiles_of(p, b, cap);
+        mine += nt;
+        if (nt == 0 && b % P == cta) {
+            uint4 *o = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + static_cast<size_t>(b) * p.Hq * D);
+            for (int i = 0; i < p.Hq * D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    const long long total = block_sum(mine, scan) * p.Hkv;
+    const long long lo = total * cta / P, hi = total * (cta + 1) / P;
+
+    // ---- pass 2: the (b, g, t) of tile `lo` ----
+    if (tid == 0) scan[16] = -1;
+    __syncthreads();
+    if (lo < hi) {
+        long long running = 0;  // tiles of sequences before this chunk, times Hkv
+        for (int base = 0; base < p.B; base += kThreads) {
+            const int b = base + tid;
+            const int nt = b < p.B ? ntiles_of(p, b, cap) : 0;
+            long long v = nt;  // inclusive scan of nt across the block
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long x = __shfl_up_sync(kFull, v, o);
+                if (lane >= o) v += x;
+            }
+            if (lane == 31) scan[warp] = v;
+            __syncthreads();
+            long long before = 0, chunk_total = 0;
+            for (int i = 0; i < kThreads / 32; ++i) {
+                if (i < warp) before += scan[i];
+                chunk_total += scan[i];
+            }
+            const long long excl = running + (before + v - nt) * p.Hkv;
+            if (nt > 0 && excl <= lo && lo < excl + static_cast<long long>(nt) * p.Hkv) {
+                scan[16] = b;
+                scan[17] = excl;
+            }
+            running += chunk_total * p.Hkv;
+            __syncthreads();
+            if (running > lo) break;  // uniform: every thread sees the same `running`
+        }
+    }
+    __syncthreads();
+    const int b0 = static_cast<int>(scan[16]);
+    const long long seq_start = scan[17];  // global index of tile (b0, 0, 0)
+
+    if (tid == 0) {
+        SegRecord r{};
+        r.lo = lo;
+        r.hi = hi;
+        r.total = total;
+        r.b = -1;
+        if (lo < hi && b0 >= 0) {
+            const int nt = ntiles_of(p, b0, cap);
+            const long long off = lo - seq_start;
+            r.b = b0;
+            r.g = static_cast<int>(off / nt);
+            r.ntiles = nt;
+            r.pair_start = seq_start + static_cast<long long>(r.g) * nt;
+        }
+        p.rec[cta] = r;
+    }
+    if (lo >= hi || b0 < 0) return;
+    const long long count = hi - lo;
+
+    if (warp == 0) {
+        // ======================= producer =======================
+        prefetch_tmap(&p.tmap_k);
+        prefetch_tmap(&p.tmap_v);
+        const int R = p.box_rows, nbox = kTN / R;
+        const uint32_t box_bytes = static_cast<uint32_t>(R) * D * 2;
+        // walker: the next tile to prepare
+        int b = b0;
+        int nt = ntiles_of(p, b, cap);
+        int n = p.context_lens[b];
+        long long off = lo - seq_start;
+        int g = static_cast<int>(off / nt), t = static_cast<int>(off % nt);
+        // the prepared tile: its coordinates and the block ids of this lane's boxes (lane l takes
+        // boxes l, l + 32, l + 64, l + 96). Preparing tile i+1 right after issuing tile i puts the
+        // block-table loads in flight while the producer waits for a free stage.
+        int pb_ = 0, pg = 0, pt = 0, pn = 0, pnt = 0, pid[4];
+        auto prepare = [&]() {
+            pb_ = b; pg = g; pt = t; pn = n; pnt = nt;
+            const int pos0 = t * kTN;
+            const int nvalid = min(kTN, n - pos0);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int k = lane + 32 * k4;
+                pid[k4] = -2;  // no box
+                if (k < nbox && k * R < nvalid)
+                    pid[k4] = p.block_tables[static_cast<size_t>(b) * p.max_blocks +
+                                             p.geom.block_of(pos0 + k * R)];
+            }
+            if (++t == nt) {
+                t = 0;
+                if (++g == p.Hkv) {
+                    g = 0;
+                    do {
+                        ++b;
+                    } while (b < p.B && (nt = ntiles_of(p, b, cap)) == 0);
+                    if (b < p.B) n = p.context_lens[b];
+                }
+            }
+        };
+        prepare();
+        int seg_t0 = 0;  // first tile of the current segment within its pair
+        bool first_seg = true;
+        long long issued = 0;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (long long i = 0; i < count; ++i) {
+            if (__shfl_sync(kFull, lane == 0 ? *abort_flag : 0, 0)) break;  // warp-uniform
+            // every lane waits and the warp reconverges before going on (a lane-0-only wait
+            // leaves the warp split for the rest of the iteration)
+            const bool ok = warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag);
+            if (!ok) {
+                if (lane == 0) {
+                    raise_err(p.err, PA_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            const int pos0 = pt * kTN;
+            const int nvalid = min(kTN, pn - pos0);
+            int slots[4];
+            unsigned long long vm[2] = {0ull, 0ull};
+            uint32_t bytes = 0;
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int k = lane + 32 * k4;
+                slots[k4] = -1;
+                if (pid[k4] == -2) continue;
+                if (pid[k4] >= 0 && pid[k4] < p.num_blocks) {
+                    slots[k4] = pid[k4] * p.geom.block_size + p.geom.offset_of(pos0 + k * R);
+                    const int r0 = k * R, r1 = r0 + min(R, nvalid - r0);  // rows [r0, r1)
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        const int a = max(r0, 64 * w), e = min(r1, 64 * w + 64);
+                        if (a < e)
+                            vm[w] |= (e - a == 64 ? ~0ull : ((1ull << (e - a)) - 1)) << (a - 64 * w);
+                    }
+                    bytes += 2 * box_bytes;
+                } else {
+                    raise_err(p.err, PA_DEVERR_TABLE);
+                }
+            }
+            unsigned vw[4];
+            vw[0] = __reduce_or_sync(kFull, static_cast<unsigned>(vm[0]));
+            vw[1] = __reduce_or_sync(kFull, static_cast<unsigned>(vm[0] >> 32));
+            vw[2] = __reduce_or_sync(kFull, static_cast<unsigned>(vm[1]));
+            vw[3] = __reduce_or_sync(kFull, static_cast<unsigned>(vm[1] >> 32));
+            bytes = __reduce_add_sync(kFull, bytes);
+            const bool last = (i == count - 1) || (pt == pnt - 1);
+            const bool first = (i == 0) || (pt == 0);
+            if (first) seg_t0 = pt;
+            int flags = (first ? kFirst : 0) | (last ? kLast : 0);
+            if (last && seg_t0 == 0 && pt == pnt - 1) flags |= kWhole;
+            if (!first_seg) flags |= kSlot1;
+            if (first) bytes += S::Q_BYTES;
+
+            unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
+            if (lane == 0) {
+                TileMeta m;
+                m.b = pb_;
+                m.g = pg;
+                m.flags = flags;
+                m.all_valid = (vw[0] & vw[1] & vw[2] & vw[3]) == 0xffffffffu;
+                m.valid[0] = (static_cast<unsigned long long>(vw[1]) << 32) | vw[0];
+                m.valid[1] = (static_cast<unsigned long long>(vw[3]) << 32) | vw[2];
+                metas[stage] = m;
+                mbar_arrive_expect_tx(full0 + 8 * stage, bytes);
+            }
+            __syncwarp();
+            const uint32_t kdst = smem_addr(st), vdst = kdst + S::TILE_BYTES;
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int k = lane + 32 * k4;
+                if (slots[k4] >= 0) {
+                    tma_load_3d(kdst + k * box_bytes, &p.tmap_k, 0, pg, slots[k4], full0 + 8 * stage);
+                    tma_load_3d(vdst + k * box_bytes, &p.tmap_v, 0, pg, slots[k4], full0 + 8 * stage);
+                }
+            }
+            if (first && lane == 0) {
+                const T *qsrc = static_cast<const T *>(p.q) + (static_cast<size_t>(pb_) * p.Hq + pg * G) * D;
+                bulk_load(kdst + 2 * S::TILE_BYTES, qsrc, S::Q_BYTES, full0 + 8 * stage);
+            }
+            ++issued;
+            if (last) first_seg = false;
+            if (++stage == NS) {
+                stage = 0;
+                phase ^= 1;
+            }
+            if (i + 1 < count) prepare();
+        }
+        // no copy may still be in flight when the CTA exits
+        if (lane == 0) {
+            const long long from = issued > NS ? issued - NS : 0;
+            for (long long i = from; i < issued; ++i) {
+                if (!mbar_wait(full0 + 8 * static_cast<int>(i % NS), static_cast<uint32_t>((i / NS) & 1))) {
+                    raise_err(p.err, PA_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+            }
         }
         return;
     }
-    const int start = split * p.chunk;
-    if (start >= n) return;
-    const int end = min(start + p.chunk, n);
-    const int nsplit = (n + p.chunk - 1) / p.chunk;
-    const int ntiles = (end - start + kTN - 1) / kTN;
 
-    // this chunk's block-table entries, checked once
-    const int b0 = p.geom.block_of(start);
-    const int nb = p.geom.block_of(end - 1) - b0 + 1;
-    const int32_t *trow = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
-    int bad = 0;
-    for (int i = tid; i < nb; i += kThreads) {
-        int id = trow[b0 + i];
-        if (id < 0 || id >= p.num_blocks) {
-            bad = 1;
-            id = -1;
-        }
-        tbl[i] = id;
-    }
-    bad = __syncthreads_or(bad);
-    if (bad && tid == 0) raise_err(p.err, PA_DEVERR_TABLE);
-
-    // query rows of the group, scaled into log2 units
+    // ========================= consumers =========================
+    const int cw = warp - 1;  // 0..7
     const int r = lane % S::LPP;
-    float qf[G][S::CPL][8];
-    {
-        const T *qb = static_cast<const T *>(p.q) + (static_cast<size_t>(b) * p.Hq + hq0) * D;
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int c = 0; c < S::CPL; ++c) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(qb + h * D + (c * S::LPP + r) * 8);
-                unpack8<E>(u, qf[h][c]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) qf[h][c][e] *= p.scale_log2;
-            }
-    }
-
-    const T *kcache = static_cast<const T *>(p.k_cache);
-    const T *vcache = static_cast<const T *>(p.v_cache);
-    auto load_tile = [&](int stage, int t) {
-        const int t0 = start + t * kTN;
-        const uint32_t kbase = smem_addr(ks + stage * S::TILE_BYTES);
-        const uint32_t vbase = smem_addr(vs + stage * S::TILE_BYTES);
-#pragma unroll
-        for (int i = 0; i < S::LOADS; ++i) {
-            const int id = tid + i * kThreads;
-            const int row = id / S::NCH, ch = id % S::NCH;
-            const int pos = t0 + row;
-            int blk = -1;
-            if (pos < end) blk = tbl[p.geom.block_of(pos) - b0];
-            const bool ok = blk >= 0;
-            const size_t slot =
-                ok ? static_cast<size_t>(blk) * p.geom.block_size + p.geom.offset_of(pos) : 0;
-            const size_t off = (slot * p.Hkv + g) * D + ch * 8;
-            cp_async16(kbase + row * D * 2 + ((ch ^ S::swz(row)) * 16), kcache + off, ok ? 16 : 0);
-            cp_async16(vbase + row * D * 2 + ch * 16, vcache + off, ok ? 16 : 0);
-        }
-    };
-
-    float m_run[G], l_part[G], acc[G][8];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m_run[h] = -INFINITY;
-        l_part[h] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[h][e] = 0.f;
-    }
-
-#pragma unroll
-    for (int s = 0; s < S::STAGES - 1; ++s) {
-        if (s < ntiles) load_tile(s, s);
-        cp_async_commit();
-    }
-
     const int rg = lane / S::LPR, cc = lane % S::LPR;
-    float *sb = sbuf + warp * G * kWPos;
-    float *pb = pbuf + warp * G * kWPos;
+    // softmax: lane handles row spos of heads shead + HPR * k (HPR = 32 / rows per warp)
+    const int spos = lane % kWPos, shead = lane / kWPos;
+    float *sb = sbuf + cw * G * kWPos;
+    float *pb = pbuf + cw * G * kWPos;
+    float *ab = abuf + cw * G;
 
-    for (int t = 0; t < ntiles; ++t) {
-        cp_async_wait<S::STAGES - 2>();
-        __syncthreads();
-        {
-            const int nt = t + S::STAGES - 1;
-            if (nt < ntiles) load_tile(nt % S::STAGES, nt);
-            cp_async_commit();
+    uint64_t q2[G][S::CPL][4];
+    uint64_t acc[G][S::NPV];
+    float m_run[S::ROUNDS], l_part[S::ROUNDS];
+    int seg = 0;  // segments finished (parity of the consumer barriers)
+    int stage = 0;
+    uint32_t phase = 0;
+
+    for (long long i = 0; i < count; ++i) {
+        bool ok = warp_wait(full0 + 8 * stage, phase, abort_flag);
+        if (!ok) {
+            if (lane == 0) {
+                raise_err(p.err, PA_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            return;
         }
-        const int stage = t % S::STAGES;
-        const int t0 = start + t * kTN;
-        const uint32_t kb = smem_addr(ks + stage * S::TILE_BYTES);
-        const uint32_t vb = smem_addr(vs + stage * S::TILE_BYTES);
+        const TileMeta &m = metas[stage];
+        const int mflags = m.flags, mb = m.b, mg = m.g, mall = m.all_valid;
+        const unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
+        const uint32_t kb = smem_addr(st), vb = kb + S::TILE_BYTES;
+        // this warp's rows as a validity mask (bit rl: row rl of the warp)
+        const unsigned vrows = warp_rows_valid(m, cw);
 
-        // scores of this warp's 16 positions
+        if (mflags & kFirst) {
+            const T *qs = reinterpret_cast<const T *>(st + 2 * S::TILE_BYTES);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int c = 0; c < S::CPL; ++c) {
+                    const int j = S::chunk(c, r, (lane / S::LPP));
+                    const uint4 u = *reinterpret_cast<const uint4 *>(qs + h * D + j * 8);
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = E::unpack2(w[e]);
+                        q2[h][c][e] = f2_pack(f.x * p.scale_log2, f.y * p.scale_log2);
+                    }
+                }
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < S::NPV; ++e) acc[h][e] = 0;
+#pragma unroll
+            for (int k = 0; k < S::ROUNDS; ++k) {
+                m_run[k] = -INFINITY;
+                l_part[k] = 0.f;
+            }
+        }
+
+        // ---- scores of this warp's 16 rows ----
 #pragma unroll
         for (int pass = 0; pass < S::PASSES; ++pass) {
-            const int pl = pass * S::PPP + lane / S::LPP;
-            const int row = warp * kWPos + pl;
-            float dot[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) dot[h] = 0.f;
+            const int u = lane / S::LPP;
+            const int rl = pass * S::PPP + u;  // row within the warp's 16
+            const int row = cw * kWPos + rl;
+            uint64_t d2[G][S::CPL];
 #pragma unroll
             for (int c = 0; c < S::CPL; ++c) {
-                const int j = c * S::LPP + r;
-                const uint4 u = lds128(kb + row * D * 2 + ((j ^ S::swz(row)) * 16));
-                float kf[8];
-                unpack8<E>(u, kf);
+                const uint4 kv = lds128(kb + row * D * 2 + S::chunk(c, r, u) * 16);
+                const uint64_t k0 = unpack_pair<E>(kv.x), k1 = unpack_pair<E>(kv.y);
+                const uint64_t k2 = unpack_pair<E>(kv.z), k3 = unpack_pair<E>(kv.w);
 #pragma unroll
-                for (int h = 0; h < G; ++h)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) dot[h] = fmaf(qf[h][c][e], kf[e], dot[h]);
+                for (int h = 0; h < G; ++h) {
+                    uint64_t a = f2_mul(q2[h][c][0], k0);
+                    a = f2_fma(q2[h][c][1], k1, a);
+                    a = f2_fma(q2[h][c][2], k2, a);
+                    d2[h][c] = f2_fma(q2[h][c][3], k3, a);
+                }
             }
-#pragma unroll
-            for (int off = S::LPP / 2; off >= 1; off >>= 1)
-#pragma unroll
-                for (int h = 0; h < G; ++h) dot[h] += __shfl_xor_sync(kFull, dot[h], off);
-            const int pos = t0 + row;
-            bool valid = pos < end;
-            if (bad && valid) valid = tbl[p.geom.block_of(pos) - b0] >= 0;
-            if (r == 0)
-#pragma unroll
-                for (int h = 0; h < G; ++h) sb[h * kWPos + pl] = valid ? dot[h] : -INFINITY;
-        }
-        __syncwarp();
-
-        // online softmax; lanes 16..31 mirror lanes 0..15 so every lane keeps the running max
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float s = sb[h * kWPos + (lane & 15)];
-            float mt = s;
-#pragma unroll
-            for (int off = 8; off >= 1; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, off));
-            const float m_new = fmaxf(m_run[h], mt);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = fast_exp2(m_run[h] - m_use);
-            m_run[h] = m_new;
-            const float pr = fast_exp2(s - m_use);
-            l_part[h] = l_part[h] * alpha + (lane < 16 ? pr : 0.f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[h][e] *= alpha;
-            if (lane < 16) pb[h * kWPos + lane] = pr;
-        }
-        __syncwarp();
-
-        // O += P V
-#pragma unroll
-        for (int it = 0; it < kWPos / S::RPI; ++it) {
-            const int pl = it * S::RPI + rg;
-            const int row = warp * kWPos + pl;
-            const uint4 u = lds128(vb + row * D * 2 + cc * 16);
-            float vf[8];
-            unpack8<E>(u, vf);
+            float dot[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                const float ph = pb[h * kWPos + pl];
+                // pairwise tree over the chunks keeps the dependency chain short
+                uint64_t t2 = d2[h][0];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(ph, vf[e], acc[h][e]);
+                for (int c = 1; c < S::CPL; ++c) t2 = f2_add(t2, d2[h][c]);
+                dot[h] = f2_lo(t2) + f2_hi(t2);
+            }
+#pragma unroll
+            for (int o = S::LPP / 2; o >= 1; o >>= 1)
+#pragma unroll
+                for (int h = 0; h < G; ++h) dot[h] += __shfl_xor_sync(kFull, dot[h], o);
+            if (r == 0) {
+                const bool valid = (vrows >> rl) & 1u;
+#pragma unroll
+                for (int h = 0; h < G; ++h) sb[h * kWPos + rl] = valid ? dot[h] : -INFINITY;
             }
         }
-    }
-    cp_async_wait<0>();
-    __syncthreads();
+        __syncwarp();
 
-    // warp totals: sum l over lanes, sum O over row groups
+        // ---- online softmax over the 16 rows ----
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
+        for (int k = 0; k < S::ROUNDS; ++k) {
+            const int h = shead + S::HPR * k;
+            const bool act = h < G;
+            const float s = act ? sb[h * kWPos + spos] : -INFINITY;
+            float mt = s;
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) l_part[h] += __shfl_xor_sync(kFull, l_part[h], off);
-#pragma unroll
-        for (int off = S::LPR; off < 32; off <<= 1)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[h][e] += __shfl_xor_sync(kFull, acc[h][e], off);
-    }
-    float *red_o = reinterpret_cast<float *>(ks);   // [warps][G][D]
-    float *red_ml = red_o + kWarps * G * D;         // [warps][G][2]
-    if (rg == 0)
+            for (int o = kWPos / 2; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, o));
+            const float m_new = fmaxf(m_run[k], mt);
+            const float mu = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = fast_exp2(m_run[k] - mu);
+            m_run[k] = m_new;
+            const float pr = fast_exp2(s - mu);
+            l_part[k] = fmaf(l_part[k], alpha, pr);
+            if (act) {
+                pb[h * kWPos + spos] = pr;
+                if (spos == 0) ab[h] = alpha;
+            }
+        }
+        __syncwarp();
+
+        // ---- O = alpha O + P V ----
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float4 *dst = reinterpret_cast<float4 *>(red_o + (warp * G + h) * D + cc * 8);
-            dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-            dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
-        }
-    if (lane == 0)
+            const float al = ab[h];
+            const uint64_t a2 = f2_pack(al, al);
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            red_ml[(warp * G + h) * 2] = m_run[h];
-            red_ml[(warp * G + h) * 2 + 1] = l_part[h];
+            for (int e = 0; e < S::NPV; ++e) acc[h][e] = f2_mul(acc[h][e], a2);
         }
-    __syncthreads();
-
-    for (int idx = tid; idx < G * D; idx += kThreads) {
-        const int h = idx / D, d = idx % D;
-        float M = -INFINITY;
+        auto pv_row = [&](int rl) {
+            const int row = cw * kWPos + rl;
+            uint64_t v[S::NPV];
+            if constexpr (S::CPV == 8) {
+                const uint4 vv = lds128(vb + row * D * 2 + cc * 16);
+                v[0] = unpack_pair<E>(vv.x);
+                v[1] = unpack_pair<E>(vv.y);
+                v[2] = unpack_pair<E>(vv.z);
+                v[3] = unpack_pair<E>(vv.w);
+            } else {
+                const uint2 vv = lds64(vb + row * D * 2 + cc * 8);
+                v[0] = unpack_pair<E>(vv.x);
+                v[1] = unpack_pair<E>(vv.y);
+            }
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_ml[(w * G + h) * 2]);
-        const float mu = M == -INFINITY ? 0.f : M;
-        float L = 0.f, O = 0.f;
+            for (int h = 0; h < G; ++h) {
+                const float pr = pb[h * kWPos + rl];
+                const uint64_t p2 = f2_pack(pr, pr);
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float sc = fast_exp2(red_ml[(w * G + h) * 2] - mu);
-            L = fmaf(red_ml[(w * G + h) * 2 + 1], sc, L);
-            O = fmaf(red_o[(w * G + h) * D + d], sc, O);
-        }
-        const float o = L > 0.f ? O / L : 0.f;
-        const size_t bh = static_cast<size_t>(b) * p.Hq + hq0 + h;
-        if (nsplit == 1) {
-            static_cast<T *>(p.out)[bh * D + d] = T(o);
+                for (int e = 0; e < S::NPV; ++e) acc[h][e] = f2_fma(p2, v[e], acc[h][e]);
+            }
+        };
+        if (mall) {
+#pragma unroll
+            for (int it = 0; it < S::PV_IT; ++it) pv_row(it * S::RPI + rg);
         } else {
-            p.ws_o[(bh * p.max_splits + split) * D + d] = o;
-            if (d == 0) {
-                p.ws_ml[(bh * p.max_splits + split) * 2] = M;
-                p.ws_ml[(bh * p.max_splits + split) * 2 + 1] = L;
+            // rows outside the context are skipped: their stage bytes may hold anything
+#pragma unroll
+            for (int it = 0; it < S::PV_IT; ++it) {
+                const int rl = it * S::RPI + rg;
+                if ((vrows >> rl) & 1u) pv_row(rl);
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+        if (++stage == NS) {
+            stage = 0;
+            phase ^= 1;
+        }
+
+        if (!(mflags & kLast)) continue;
+
+        // ---- end of a segment: combine the 8 warps ----
+        float *ro = red + cw * G * (D + 2);
+#pragma unroll
+        for (int k = 0; k < S::ROUNDS; ++k) {
+            float l = l_part[k];
+#pragma unroll
+            for (int o = kWPos / 2; o >= 1; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
+            const int h = shead + S::HPR * k;
+            if (h < G && spos == 0) {
+                ro[h * (D + 2) + D] = m_run[k];
+                ro[h * (D + 2) + D + 1] = l;
+            }
+        }
+#pragma unroll
+        for (int o = S::LPR; o < 32; o <<= 1)
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < S::NPV; ++e) {
+                    const float lo_ = f2_lo(acc[h][e]) + __shfl_xor_sync(kFull, f2_lo(acc[h][e]), o);
+                    const float hi_ = f2_hi(acc[h][e]) + __shfl_xor_sync(kFull, f2_hi(acc[h][e]), o);
+                    acc[h][e] = f2_pack(lo_, hi_);
+                }
+        if (rg == 0)
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float *dst = ro + h * (D + 2) + cc * S::CPV;
+#pragma unroll
+                for (int e = 0; e < S::NPV; ++e) {
+                    dst[2 * e] = f2_lo(acc[h][e]);
+                    dst[2 * e + 1] = f2_hi(acc[h][e]);
+                }
+            }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cons0);
+        ok = warp_wait(cons0, seg & 1, abort_flag);
+        if (!ok) {
+            if (lane == 0) {
+                raise_err(p.err, PA_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            return;
+        }
+        const int ct = cw * 32 + lane;
+        const size_t bh = static_cast<size_t>(mb) * p.Hq + static_cast<size_t>(mg) * G;
+        float *part = p.part + (static_cast<size_t>(cta) * 2 + ((mflags & kSlot1) ? 1 : 0)) * G * (D + 2);
+        for (int idx = ct; idx < G * D; idx += kConsThreads) {
+            const int h = idx / D, d = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, red[(w * G + h) * (D + 2) + D]);
+            const float mu = M == -INFINITY ? 0.f : M;
+            float L = 0.f, O = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) {
+                const float *rw = red + (w * G + h) * (D + 2);
+                const float sc = fast_exp2(rw[D] - mu);
+                L = fmaf(rw[D + 1], sc, L);
+                O = fmaf(rw[d], sc, O);
+            }
+            const float o = L > 0.f ? O / L : 0.f;
+            if (mflags & kWhole) {
+                static_cast<T *>(p.out)[(bh + h) * D + d] = T(o);
+            } else {
+                part[h * (D + 2) + d] = o;
+                if (d == 0) {
+                    part[h * (D + 2) + D] = M;
+                    part[h * (D + 2) + D + 1] = L;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cons0 + 8);
+        ok = warp_wait(cons0 + 8, seg & 1, abort_flag);
+        if (!ok) {
+            if (lane == 0) {
+                raise_err(p.err, PA_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            return;
+        }
+        ++seg;
     }
 }
 
-// One warp per (sequence, query head): combine the splits' normalised partials.
-template <int D, class E>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p) {
+// One CTA per decode CTA: if that CTA's first pair began in an earlier CTA and ends in this one,
+// combine the pair's partial segments into the output.
+template <int D, int G, class E>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ DecodeParams p) {
     using T = typename E::T;
-    constexpr int PER = D / 32;  // output columns per lane
-    const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (wid >= p.B * p.Hq) return;
-    const int b = wid / p.Hq;
-    const int n = p.context_lens[b];
-    const long long cap = static_cast<long long>(p.max_blocks) * p.geom.block_size;
-    if (n <= 0 || n > cap) return;  // the split kernel wrote zeros
-    const int nsplit = (n + p.chunk - 1) / p.chunk;
-    if (nsplit <= 1) return;  // the split kernel wrote the output
-
-    const float *ml = p.ws_ml + static_cast<size_t>(wid) * p.max_splits * 2;
-    const float *os = p.ws_o + static_cast<size_t>(wid) * p.max_splits * D;
-    float M = -INFINITY;
-    for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, ml[2 * s]);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-    const float mu = M == -INFINITY ? 0.f : M;
-
-    float W = 0.f, o[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) o[e] = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-        const float w = ml[2 * s + 1] * fast_exp2(ml[2 * s] - mu);
-        W += w;
-        const float *src = os + static_cast<size_t>(s) * D + lane * PER;
-        if constexpr (PER == 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(src);
-            o[0] = fmaf(w, x.x, o[0]); o[1] = fmaf(w, x.y, o[1]);
-            o[2] = fmaf(w, x.z, o[2]); o[3] = fmaf(w, x.w, o[3]);
-        } else {
-            const float2 x = *reinterpret_cast<const float2 *>(src);
-            o[0] = fmaf(w, x.x, o[0]); o[1] = fmaf(w, x.y, o[1]);
+    const int c = blockIdx.x, P = gridDim.x;
+    const SegRecord rc = p.rec[c];
+    if (rc.b < 0 || rc.pair_start >= rc.lo || rc.pair_start + rc.ntiles > rc.hi) return;
+    // first CTA whose range holds the pair's first tile: max{c' : lo(c') <= pair_start}
+    const long long x = rc.pair_start;
+    int c0 = static_cast<int>(((x + 1) * P + rc.total - 1) / rc.total) - 1;
+    if (c0 < 0) c0 = 0;
+    const size_t bh = static_cast<size_t>(rc.b) * p.Hq + static_cast<size_t>(rc.g) * G;
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+        const int h = idx / D, d = idx % D;
+        float M = -INFINITY;
+        for (int cc = c0; cc <= c; ++cc) {
+            const SegRecord r = p.rec[cc];
+            if (r.lo >= r.hi) continue;
+            const int slot = (cc == c0 && r.lo < x) ? 1 : 0;
+            M = fmaxf(M, p.part[((static_cast<size_t>(cc) * 2 + slot) * G + h) * (D + 2) + D]);
         }
+        const float mu = M == -INFINITY ? 0.f : M;
+        float L = 0.f, O = 0.f;
+        for (int cc = c0; cc <= c; ++cc) {
+            const SegRecord r = p.rec[cc];
+            if (r.lo >= r.hi) continue;
+            const int slot = (cc == c0 && r.lo < x) ? 1 : 0;
+            const float *pp = p.part + ((static_cast<size_t>(cc) * 2 + slot) * G + h) * (D + 2);
+            const float w = pp[D + 1] * fast_exp2(pp[D] - mu);
+            L += w;
+            O = fmaf(w, pp[d], O);
+        }
+        static_cast<T *>(p.out)[(bh + h) * D + d] = T(L > 0.f ? O / L : 0.f);
     }
-    const float inv = W > 0.f ? 1.f / W : 0.f;
-    uint32_t packed[PER / 2];
-#pragma unroll
-    for (int e = 0; e < PER / 2; ++e) packed[e] = E::pack2(o[2 * e] * inv, o[2 * e + 1] * inv);
-    T *dst = static_cast<T *>(p.out) + static_cast<size_t>(wid) * D + lane * PER;
-    if constexpr (PER == 4)
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
-    else
-        *reinterpret_cast<uint32_t *>(dst) = packed[0];
+}
+
+// ------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+bool encode_pool(CUtensorMap *m, const void *pool, pa_dtype dt, int D, int Hkv, long long slots,
+                 int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+                          static_cast<cuuint64_t>(slots > 0 ? slots : 1)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hkv) * D * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+              const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int G>
+constexpr int stages_for() {
+    const int budget = kSmemPerSm / ctas_per_sm<G>() - 1024;
+    const int s = (budget - fixed_smem<D, G>()) / Shape<D, G>::STAGE_BYTES;
+    return s < 6 ? s : 6;
 }
 
 template <int D, int G, class E>
-cudaError_t launch_typed(const DecodeParams &prm, const DecodePlan &plan, cudaStream_t stream) {
-    const int smem = smem_bytes_for<D, G>(plan.tbl_cap);
-    auto kern = decode_split_kernel<D, G, E>;
-    static int configured_smem = 0;  // per instantiation; raised once per size
-    if (smem > configured_smem) {
+cudaError_t launch_typed(DecodeParams &prm, cudaStream_t stream) {
+    static_assert(stages_for<D, G>() >= 2, "the ring needs two stages");
+    prm.stages = stages_for<D, G>();
+    const int smem = prm.stages * Shape<D, G>::STAGE_BYTES + fixed_smem<D, G>();
+    auto kern = decode_kernel<D, G, E>;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (configured[dev] < smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        configured_smem = smem;
+        configured[dev] = smem;
     }
-    dim3 grid(plan.max_splits, prm.Hkv, prm.B);
-    kern<<<grid, kThreads, smem, stream>>>(prm);
+    const int P = device_sm_count() * ctas_per_sm<G>();
+    kern<<<P, kThreads, smem, stream>>>(prm);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || plan.max_splits <= 1) return e;
-    const int warps = prm.B * prm.Hq;
-    decode_merge_kernel<D, E><<<(warps + 3) / 4, 128, 0, stream>>>(prm);
+    if (e != cudaSuccess) return e;
+    decode_merge_kernel<D, G, E><<<P, 128, 0, stream>>>(prm);
     return cudaGetLastError();
 }
 
 template <int D, class E>
-cudaError_t dispatch_group(int G, const DecodeParams &prm, const DecodePlan &plan,
-                           cudaStream_t stream) {
+cudaError_t dispatch_group(int G, DecodeParams &prm, cudaStream_t stream) {
     switch (G) {
-        case 1: return launch_typed<D, 1, E>(prm, plan, stream);
-        case 2: return launch_typed<D, 2, E>(prm, plan, stream);
-        case 3: return launch_typed<D, 3, E>(prm, plan, stream);
-        case 4: return launch_typed<D, 4, E>(prm, plan, stream);
-        case 5: return launch_typed<D, 5, E>(prm, plan, stream);
-        case 6: return launch_typed<D, 6, E>(prm, plan, stream);
-        case 7: return launch_typed<D, 7, E>(prm, plan, stream);
-        case 8: return launch_typed<D, 8, E>(prm, plan, stream);
+        case 1: return launch_typed<D, 1, E>(prm, stream);
+        case 2: return launch_typed<D, 2, E>(prm, stream);
+        case 3: return launch_typed<D, 3, E>(prm, stream);
+        case 4: return launch_typed<D, 4, E>(prm, stream);
+        case 5: return launch_typed<D, 5, E>(prm, stream);
+        case 6: return launch_typed<D, 6, E>(prm, stream);
+        case 7: return launch_typed<D, 7, E>(prm, stream);
+        case 8: return launch_typed<D, 8, E>(prm, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -406,58 +777,52 @@ cudaError_t dispatch_group(int G, const DecodeParams &prm, const DecodePlan &pla
 }  // namespace
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int block_size) {
+    (void)B;
+    (void)max_blocks_per_seq;
+    (void)block_size;
     DecodePlan plan{};
-    const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
-    const long long tiles_max = (max_ctx + kTN - 1) / kTN;
-    const int ctas_per_sm = D == 128 ? 2 : 3;
-    const long long target = static_cast<long long>(device_sm_count()) * ctas_per_sm * 4;
-    const long long pairs = static_cast<long long>(B) * Hkv;
-    // guess the mean context as half the maximum; cut chunks so ~4 waves of CTAs exist, but
-    // never let one CTA stream more than ~256 KB (tail) or less than one tile
-    const long long expect_tiles = pairs * ((tiles_max + 1) / 2);
-    long long tpc = (expect_tiles + target - 1) / (target > 0 ? target : 1);
-    const long long tpc_max = D == 128 ? 8 : 16;
-    if (tpc < 1) tpc = 1;
-    if (tpc > tpc_max) tpc = tpc_max;
-    plan.chunk = static_cast<int>(tpc * kTN);
-    plan.max_splits = max_ctx > 0 ? static_cast<int>((max_ctx + plan.chunk - 1) / plan.chunk) : 1;
-    plan.tbl_cap = plan.chunk / block_size + 2;
-    plan.ws_bytes = plan.max_splits > 1
-                        ? static_cast<size_t>(B) * Hq * plan.max_splits * (D + 2) * sizeof(float)
-                        : 0;
+    const int G = Hq / Hkv;
+    const size_t P = static_cast<size_t>(device_sm_count()) * (G <= 3 ? 2 : 1);
+    const size_t part = P * 2 * G * (D + 2) * sizeof(float);
+    plan.ws_bytes = (part + 255) / 256 * 256 + P * sizeof(SegRecord);
     return plan;
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream) {
     if (a.B == 0) return cudaSuccess;
     DecodeParams prm{};
+    // rows per TMA box: the largest power of two dividing both the block size and the tile
+    int R = 1;
+    while (R < kTN && a.block_size % (2 * R) == 0) R *= 2;
+    const long long slots = static_cast<long long>(a.num_blocks) * a.block_size;
+    if (!encode_pool(&prm.tmap_k, a.k_cache, a.dtype, a.D, a.Hkv, slots, R) ||
+        !encode_pool(&prm.tmap_v, a.v_cache, a.dtype, a.D, a.Hkv, slots, R))
+        return cudaErrorInvalidValue;
     prm.q = a.q;
-    prm.k_cache = a.k_cache;
-    prm.v_cache = a.v_cache;
     prm.block_tables = a.block_tables;
     prm.context_lens = a.context_lens;
     prm.out = a.out;
-    float *ws = static_cast<float *>(a.workspace);
-    prm.ws_o = ws;
-    prm.ws_ml = ws ? ws + static_cast<size_t>(a.B) * a.Hq * plan.max_splits * a.D : nullptr;
+    const int G = a.Hq / a.Hkv;
+    const size_t P = static_cast<size_t>(device_sm_count()) * (G <= 3 ? 2 : 1);
+    const size_t part = P * 2 * G * (a.D + 2) * sizeof(float);
+    prm.part = static_cast<float *>(a.workspace);
+    prm.rec = reinterpret_cast<SegRecord *>(static_cast<char *>(a.workspace) + (part + 255) / 256 * 256);
+    (void)plan;
     prm.err = a.err;
     prm.B = a.B;
     prm.Hq = a.Hq;
     prm.Hkv = a.Hkv;
     prm.max_blocks = a.max_blocks;
     prm.num_blocks = a.num_blocks;
-    prm.chunk = plan.chunk;
-    prm.max_splits = plan.max_splits;
-    prm.tbl_cap = plan.tbl_cap;
+    prm.box_rows = R;
     prm.geom.block_size = a.block_size;
     prm.geom.shift = log2_if_pow2(a.block_size);
     prm.scale_log2 = a.scale * kLog2e;
-    const int G = a.Hq / a.Hkv;
     if (a.D == 128)
-        return a.dtype == PA_BF16 ? dispatch_group<128, BF16>(G, prm, plan, stream)
-                                  : dispatch_group<128, F16>(G, prm, plan, stream);
-    return a.dtype == PA_BF16 ? dispatch_group<64, BF16>(G, prm, plan, stream)
-                              : dispatch_group<64, F16>(G, prm, plan, stream);
+        return a.dtype == PA_BF16 ? dispatch_group<128, BF16>(G, prm, stream)
+                                  : dispatch_group<128, F16>(G, prm, stream);
+    return a.dtype == PA_BF16 ? dispatch_group<64, BF16>(G, prm, stream)
+                              : dispatch_group<64, F16>(G, prm, stream);
 }
 
 }  // namespace pa

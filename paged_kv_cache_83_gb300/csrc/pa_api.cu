@@ -92,6 +92,7 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
         return PA_ERR_NULL;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(num_blocks) * block_size > INT_MAX) return PA_ERR_UNSUPPORTED;
     const pa::DecodePlan plan = pa::plan_decode(B, Hq, Hkv, D, max_blocks_per_seq, block_size);
     if (plan.ws_bytes > 0 && (!workspace || workspace_bytes < plan.ws_bytes || !aligned16(workspace)))
         return PA_ERR_WORKSPACE;

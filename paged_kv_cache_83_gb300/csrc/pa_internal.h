@@ -21,13 +21,10 @@ struct StoreArgs {
 cudaError_t launch_store_kv(const StoreArgs &a, cudaStream_t stream);
 
 // ------------------------------------------------------------------------------------------
-// Split-K decode. A sequence's context is cut into chunks of `chunk` positions; CTA
-// (split, kv head, sequence) handles one chunk for the whole GQA group of that kv head.
+// Decode: one persistent CTA per SM streams an equal share of the (sequence, kv head, tile)
+// space; pieces of a context shared by two CTAs are combined by a small merge kernel.
 struct DecodePlan {
-    int chunk;       // positions per split (a multiple of the 64-position tile)
-    int max_splits;  // ceil(max context / chunk)
-    int tbl_cap;     // block-table entries one chunk can span
-    size_t ws_bytes; // scratch for partial results (0 when max_splits == 1)
+    size_t ws_bytes;  // scratch: per SM two partial results and one record
 };
 DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int block_size);
 
