@@ -444,7 +444,7 @@ def bench_prefill(torch, pa, dev, stream, bf16_peak, hbm, args) -> dict:
     pf = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     flops = prefill_flops(c.q_lens, c.k_lens, c.Hq, c.D)
     st_bytes = 4 * int(c.q.shape[0]) * c.Hkv * c.D * 2
-    return {"prefill": {"workload": "prefill_prefix", "kernel": "prefill_mma_kernel",
+    return {"prefill": {"workload": "prefill_prefix", "kernel": "prefill_tc_kernel",
                         "ms": pf, "TFLOP_per_s": flops / (pf * 1e-3) / 1e12,
                         "frac_of_bf16_peak": flops / (pf * 1e-3) / 1e12 / bf16_peak,
                         "peak": bf16_peak, "flops": flops, "l2": "flushed between iterations"},

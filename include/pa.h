@@ -157,6 +157,9 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
  *               PA_DEVERR_LENGTH are zero).
  * q             [Tq, Hq, D].
  * cu_seqlens_q, cu_seqlens_k  int32 [S+1], non-decreasing, starting at 0.
+ * total_q       host int: rows of q and out (= cu_seqlens_q[S]); bounds every read of q.
+ * total_k       host int: rows of the packed k, v (= cu_seqlens_k[S]) when block_tables is NULL;
+ *               ignored otherwise.
  * max_seqlen_q  host int >= every q_len (sizes the grid); max_seqlen_k is accepted for
  *               interface parity and not needed.
  * S == 0 is a no-op.
@@ -164,10 +167,10 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
 pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void *v,
                             const void *k_cache, const void *v_cache,
                             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int S,
-                            int max_seqlen_q, int max_seqlen_k, const int32_t *block_tables,
-                            int max_blocks_per_seq, int Hq, int Hkv, int D, int block_size,
-                            int num_blocks, float scale, int causal, pa_dtype dtype,
-                            int32_t *err, cudaStream_t stream);
+                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                            const int32_t *block_tables, int max_blocks_per_seq, int Hq, int Hkv,
+                            int D, int block_size, int num_blocks, float scale, int causal,
+                            pa_dtype dtype, int32_t *err, cudaStream_t stream);
 
 /*
  * pa_decode_noalloc: pa_decode for callers that cannot allocate device memory.

@@ -46,8 +46,8 @@ def load(path: Path | str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_decode_workspace_size.restype = Z
     lib.pa_decode.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, P, Z, P, P]
     lib.pa_decode.restype = I
-    lib.pa_prefill_varlen.argtypes = [P, P, P, P, P, P, P, P, I, I, I, P, I, I, I, I, I, I, F, I,
-                                      I, P, P]
+    lib.pa_prefill_varlen.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, I, I, I, I, I, I,
+                                      F, I, I, P, P]
     lib.pa_prefill_varlen.restype = I
     lib.pa_decode_noalloc.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, P, P]
     lib.pa_decode_noalloc.restype = I
@@ -179,8 +179,9 @@ def pa_prefill_varlen(out, q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k
     for t in (out, k, v, k_cache, v_cache):
         if t is not None and t.dtype != q.dtype:
             raise TypeError("all attention tensors must share a dtype")
+    total_k = 0 if block_tables is not None else int(k.shape[0])
     _check("pa_prefill_varlen", load().pa_prefill_varlen(
         _ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
-        _i32(cu_seqlens_q, "cu_seqlens_q"), _i32(cu_seqlens_k, "cu_seqlens_k"), S,
+        _i32(cu_seqlens_q, "cu_seqlens_q"), _i32(cu_seqlens_k, "cu_seqlens_k"), S, Tq, total_k,
         int(max_seqlen_q), int(max_seqlen_k), _i32(block_tables, "block_tables"), maxb, Hq, Hkv, D,
         bs, NB, float(scale), int(bool(causal)), dt, _i32(err, "err"), _stream(stream)))

@@ -106,13 +106,15 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
 pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void *v,
                             const void *k_cache, const void *v_cache,
                             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int S,
-                            int max_seqlen_q, int max_seqlen_k, const int32_t *block_tables,
-                            int max_blocks_per_seq, int Hq, int Hkv, int D, int block_size,
-                            int num_blocks, float scale, int causal, pa_dtype dtype,
-                            int32_t *err, cudaStream_t stream) {
+                            int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                            const int32_t *block_tables, int max_blocks_per_seq, int Hq, int Hkv,
+                            int D, int block_size, int num_blocks, float scale, int causal,
+                            pa_dtype dtype, int32_t *err, cudaStream_t stream) {
     (void)max_seqlen_k;
     if (!dtype_ok(dtype)) return PA_ERR_DTYPE;
-    if (S < 0 || max_seqlen_q < 0 || (causal != 0 && causal != 1)) return PA_ERR_SHAPE;
+    if (S < 0 || max_seqlen_q < 0 || total_q < 0 || (!block_tables && total_k < 0) ||
+        (causal != 0 && causal != 1))
+        return PA_ERR_SHAPE;
     pa_status st = check_heads(Hq, Hkv, D);
     if (st != PA_OK) return st;
     if (block_tables &&
@@ -120,8 +122,10 @@ pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void 
          static_cast<long long>(max_blocks_per_seq) * block_size > INT_MAX))
         return PA_ERR_SHAPE;
     if (S > 65535) return PA_ERR_UNSUPPORTED;
-    if (S == 0 || max_seqlen_q == 0) return PA_OK;
+    if (S == 0 || max_seqlen_q == 0 || total_q == 0) return PA_OK;
     if (!out || !q || !cu_seqlens_q || !cu_seqlens_k) return PA_ERR_NULL;
+    if (block_tables && static_cast<long long>(num_blocks) * block_size > INT_MAX)
+        return PA_ERR_UNSUPPORTED;
     if (block_tables ? (!k_cache || !v_cache) : (!k || !v)) return PA_ERR_NULL;
     const void *kk = block_tables ? k_cache : k;
     const void *vv = block_tables ? v_cache : v;
@@ -138,6 +142,8 @@ pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void 
     a.cu_k = cu_seqlens_k;
     a.block_tables = block_tables;
     a.S = S;
+    a.total_q = total_q;
+    a.total_k = block_tables ? 0 : total_k;
     a.max_seqlen_q = max_seqlen_q;
     a.max_blocks = max_blocks_per_seq;
     a.Hq = Hq;

@@ -1,5 +1,6 @@
 // prefill_mma.cu: varlen causal prefill with a paged prefix (pa_prefill_varlen), warp-level
-// mma.sync version.
+// mma.sync version: the general path for the shapes the tcgen05 kernel (prefill_tc.cu) does not
+// take (head dim 64, odd group sizes, block sizes without an 8-row power-of-two divisor).
 //
 // Source: "nano-vLLM Part 4", section 3 (prefill: packed prompts, variable-length attention with
 // an optional prefix block table); smzdm nano-vLLM deep dive, "GPU执行优化" (cu_seqlens mark the
@@ -324,6 +325,7 @@ cudaError_t launch_typed(const PrefillParams &prm, cudaStream_t stream) {
 
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     if (a.S == 0 || a.max_seqlen_q == 0) return cudaSuccess;
+    if (tc_prefill_supported(a)) return launch_prefill_tc(a, stream);
     PrefillParams prm{};
     prm.q = a.q;
     prm.k = a.k;

@@ -87,9 +87,9 @@ def test_decode_host_checks(lib):
 
 
 def _prefill(lib, **kw):
-    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, S=2, mq=8, mk=8,
-             bt=FAKE, maxb=2, Hq=4, Hkv=2, D=128, bs=16, nb=8, scale=0.1, causal=1, dt=1, err=None,
-             stream=None)
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, S=2, tq=16, tk=16,
+             mq=8, mk=8, bt=FAKE, maxb=2, Hq=4, Hkv=2, D=128, bs=16, nb=8, scale=0.1, causal=1, dt=1,
+             err=None, stream=None)
     a.update(kw)
     return lib.pa_prefill_varlen(*a.values())
 
@@ -105,6 +105,8 @@ def test_prefill_host_checks(lib):
     assert _prefill(lib, bt=None, k=None) == 1       # packed keys missing
     assert _prefill(lib, cq=None) == 1
     assert _prefill(lib, bs=0) == 2
+    assert _prefill(lib, tq=-1) == 2
+    assert _prefill(lib, tq=0) == 0                   # no query rows: no-op
 
 
 def test_workspace_size_rules(lib):
