@@ -49,10 +49,14 @@ METRIC = "paged-decode KV-read GB/s (% of GB300 HBM peak); decode steps/sec per 
 DEFAULT_WORKLOAD = "qwen3_06b_decode"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic of one decode_split_kernel launch on the default workload, from the ncu capture
-# summarised in profiles/ (scaled as described there); valid only for the decode source it was
-# taken on, identified by its hash.
-DECODE_TRAFFIC = {"sha256": None, "bytes": None}
+# DRAM traffic (read + write bytes) of one launch, from the ncu captures summarised in
+# profiles/decode_kernel_qwen3_06b_decode.md and profiles/prefill_tc_kernel_prefill_prefix.md
+# (layer 0 of the default workload; prefill_prefix). Each is valid only for the kernel sources it
+# was taken on, identified by their hash; after any change the bench reports null.
+DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_279_818_544,
+                  "sha256": "7c3c73c81f58a6004f56fe6371f3895d327c3aa6815d22380a8a4201abbc2736"}
+PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 407_848_192,
+                   "sha256": "4d819b579b8c961374471c73c9a3e8b17f878a7684c477dae30451113d07ad51"}
 
 
 def peaks() -> tuple[dict, str]:
@@ -74,8 +78,15 @@ def prefill_flops(q_lens, k_lens, Hq, D) -> int:
     return tot
 
 
-def src_hash(name: str) -> str:
-    return hashlib.sha256((ROOT / "paged_kv_cache_83_gb300" / "csrc" / name).read_bytes()).hexdigest()
+def src_hash(*names: str) -> str:
+    m = hashlib.sha256()
+    for name in names:
+        m.update((ROOT / "paged_kv_cache_83_gb300" / "csrc" / name).read_bytes())
+    return m.hexdigest()
+
+
+def traffic_of(rec: dict):
+    return rec["bytes"] if src_hash(*rec["sources"]) == rec["sha256"] else None
 
 
 # ---------------------------------------------------------------------------------------------
@@ -318,8 +329,8 @@ def run_gpu(args, ws_, rank, local):
     dec_mean = statistics.mean(dec_ms)
     dec_bytes_mean = statistics.mean(nbytes[i % nl] for i in range(args.steps))
     achieved = dec_bytes_mean / (dec_mean * 1e-3) / 1e9
-    dsha = src_hash("decode.cu")
-    traffic = DECODE_TRAFFIC["bytes"] if DECODE_TRAFFIC["sha256"] == dsha else None
+    # traffic was captured on layer 0; report it for the launches on that layer
+    traffic = traffic_of(DECODE_TRAFFIC)
 
     # ---- e2e: inputs from pinned host memory each step, output read back each step ----
     L = layers[0]
@@ -447,7 +458,8 @@ def bench_prefill(torch, pa, dev, stream, bf16_peak, hbm, args) -> dict:
     return {"prefill": {"workload": "prefill_prefix", "kernel": "prefill_tc_kernel",
                         "ms": pf, "TFLOP_per_s": flops / (pf * 1e-3) / 1e12,
                         "frac_of_bf16_peak": flops / (pf * 1e-3) / 1e12 / bf16_peak,
-                        "peak": bf16_peak, "flops": flops, "l2": "flushed between iterations"},
+                        "peak": bf16_peak, "flops": flops, "l2": "flushed between iterations",
+                        "traffic": traffic_of(PREFILL_TRAFFIC)},
             "store_kv_prefill": {"kernel": "store_kv_kernel", "ms": st, "bytes": st_bytes,
                                  "GB_per_s": st_bytes / (st * 1e-3) / 1e9,
                                  "frac_of_hbm": st_bytes / (st * 1e-3) / 1e9 / hbm}}
