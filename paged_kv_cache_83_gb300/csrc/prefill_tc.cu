@@ -283,19 +283,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             tc_fence_after();
             const int n0 = j * BN;
             const bool masked = n0 + BN > lim;
-            uint32_t v[32];
-            float mx = -INFINITY;
+            uint32_t va[32], vb[32];
+            // pass 1: row maximum of the raw scores (the scale is positive, so it is applied once)
+            float ma = -INFINITY, mb2 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld32(srow + c * 32, v);
+            for (int c = 0; c < 4; c += 2) {
+                tmem_ld32(srow + c * 32, va);
+                tmem_ld32(srow + (c + 1) * 32, vb);
                 tmem_wait_ld();
+                if (masked) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        if (n0 + c * 32 + e >= lim) va[e] = 0xff800000u;        // -inf
+                        if (n0 + (c + 1) * 32 + e >= lim) vb[e] = 0xff800000u;
+                    }
+                }
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    float x = __uint_as_float(v[e]) * p.scale_log2;
-                    if (masked && n0 + c * 32 + e >= lim) x = -INFINITY;
-                    mx = fmaxf(mx, x);
+                    ma = fmaxf(ma, __uint_as_float(va[e]));
+                    mb2 = fmaxf(mb2, __uint_as_float(vb[e]));
                 }
             }
+            const float mraw = fmaxf(ma, mb2);
+            const float mx = mraw == -INFINITY ? -INFINITY : mraw * p.scale_log2;
             // move the reference max only when it grew by more than 2^8 (or was unset)
             const bool need = mx > m_use + 8.f;
             if (__any_sync(kFull, need && j > 0)) {
@@ -304,35 +314,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 const float f = need ? fast_exp2(m_use - mx) : 1.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(orow + c * 32, v);
+                    tmem_ld32(orow + c * 32, va);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * f);
-                    tmem_st32(orow + c * 32, v);
+                    for (int e = 0; e < 32; ++e) va[e] = __float_as_uint(__uint_as_float(va[e]) * f);
+                    tmem_st32(orow + c * 32, va);
                 }
                 if (need) l *= f;
             }
             if (need) m_use = mx;
             const float mu = m_use == -INFINITY ? 0.f : m_use;
+            // pass 2: p = 2^(s * scale - m) on fp32 pairs, written back as 16-bit pairs
+            const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-mu, -mu);
+            uint64_t l2 = f2_pack(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tmem_ld32(srow + c * 32, v);
+            for (int c = 0; c < 4; c += 2) {
+                tmem_ld32(srow + c * 32, va);
+                tmem_ld32(srow + (c + 1) * 32, vb);
                 tmem_wait_ld();
-                uint32_t pk[16];
+                uint32_t pk[2][16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float x0 = __uint_as_float(v[e]) * p.scale_log2;
-                    float x1 = __uint_as_float(v[e + 1]) * p.scale_log2;
-                    if (masked) {
-                        if (n0 + c * 32 + e >= lim) x0 = -INFINITY;
-                        if (n0 + c * 32 + e + 1 >= lim) x1 = -INFINITY;
+                for (int half = 0; half < 2; ++half) {
+                    const uint32_t *v = half ? vb : va;
+                    const int kb = n0 + (c + half) * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const uint64_t x2 = f2_fma(u2_pack(v[e], v[e + 1]), sc2, nm2);
+                        float x0 = f2_lo(x2), x1 = f2_hi(x2);
+                        if (masked) {
+                            if (kb + e >= lim) x0 = -INFINITY;
+                            if (kb + e + 1 >= lim) x1 = -INFINITY;
+                        }
+                        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                        l2 = f2_add(l2, f2_pack(p0, p1));
+                        pk[half][e >> 1] = E::pack2(p0, p1);
                     }
-                    const float p0 = fast_exp2(x0 - mu), p1 = fast_exp2(x1 - mu);
-                    l += p0 + p1;
-                    pk[e >> 1] = E::pack2(p0, p1);
                 }
-                tmem_st16(srow + c * 16, pk);
+                tmem_st16(srow + c * 16, pk[0]);
+                tmem_st16(srow + (c + 1) * 16, pk[1]);
             }
+            l += f2_lo(l2) + f2_hi(l2);
             tmem_wait_st();
             // the last tile may hold rows past the keys (unwritten slots or another prompt):
             // head A's warps zero those V rows before any PV reads them
