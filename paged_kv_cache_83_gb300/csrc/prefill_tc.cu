@@ -10,17 +10,19 @@
 // GQA pair), so every K/V tile it loads serves 256 rows. Shapes: head dim 128, even group sizes.
 //
 //   warp 0      producer: TMA loads of the two Q tiles, then of 128-key K and V tiles through the
-//               block table (or from the packed k, v), 128-byte swizzled, into 2-stage rings.
-//   warp 1      owns the 512 TMEM columns and issues the MMAs (one thread):
-//                 S_A = Q_A K^T, S_B = Q_B K^T           (SS: both operands in shared memory)
-//                 O_A += P_A V,  O_B += P_B V            (TS: P read from tensor memory)
-//               in the order QK_A(j+1) right after PV_A(j), so head B's softmax overlaps head A's
-//               MMAs and the other way round.
+//               block table (or from the packed k, v), 128-byte swizzled, into a 3-slot ring in
+//               the order the MMAs consume them (K0, K1, V0, K2, V1, ...).
+//   warps 1, 2  one MMA issuer per head (one thread each; warp 1 owns the 512 TMEM columns):
+//                 S_h = Q_h K^T   as soon as the softmax has read S_h of the previous tile,
+//                 O_h += P_h V    as soon as P_h is in shared memory.
+//               Both operands of both MMAs come from shared memory, so S of the next tile is
+//               computed while the softmax still works on the current one.
 //   warps 4-7   softmax of head A, warps 8-11 softmax of head B: thread = one query row = one
-//               TMEM lane. Row max over the tile (masked: causal bound P + row, context end), then
-//               P = 2^(s - m) in bf16/fp16 written back over S's first 64 columns, which the
-//               PV MMA takes as its A operand. O is rescaled in TMEM only when the row max grew
-//               by more than 2^8 (the normaliser uses the same reference, so the result is exact).
+//               TMEM lane. S is read once into registers (then released), masked (causal bound
+//               P + row, context end), row max, P = 2^(s - m) in bf16/fp16 stored to shared
+//               memory in the swizzled layout the PV MMA reads. O is rescaled in TMEM only when
+//               the row max grew by more than 2^8 (the normaliser uses the same reference, so the
+//               result is exact).
 //   TMEM columns: S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511.
 // Every wait is bounded (PA_DEVERR_TIMEOUT); on a timeout every role drains what it started
 // (TMA, MMAs) before the TMEM is freed.
@@ -38,12 +40,25 @@ constexpr int BM = 128, BN = 128, HD = 128;
 constexpr int kThreads = 384;
 constexpr int kHalf = BM * 64 * 2;  // one 128-row x 64-column half tile: 16 KB
 constexpr int kTile = 2 * kHalf;    // 128 x 128 elements: 32 KB
-constexpr int OFF_QA = 0, OFF_QB = kTile, OFF_K = 2 * kTile, OFF_V = 4 * kTile, OFF_BAR = 6 * kTile;
+constexpr int kRing = 3;            // K/V tile slots
+constexpr uint32_t kTileDesc = kTile >> 4;  // one tile further, in descriptor address units
+constexpr int OFF_QA = 0, OFF_QB = kTile, OFF_PA = 2 * kTile, OFF_PB = 3 * kTile, OFF_RING = 4 * kTile,
+              OFF_BAR = OFF_RING + kRing * kTile;
+// per-head barriers take index base + h (h = 0 for head A, 1 for head B)
 enum {
-    B_Q = 0, B_KF0, B_KF1, B_VF0, B_VF1, B_KE0, B_KE1, B_VE0, B_VE1,
-    B_SA, B_SB, B_PA, B_PB, B_OA, B_OB, B_END, NBAR
+    B_Q = 0,
+    B_FULL = 1,                // + slot: a K/V tile landed (TMA transaction count)
+    B_EMPTY = B_FULL + kRing,  // + slot: both heads' MMAs are done with it (two commits)
+    B_S = B_EMPTY + kRing,     // + h: S = Q K^T is in TMEM
+    B_F = B_S + 2,             // + h: the softmax warps have read S (4 arrivals)
+    B_P = B_F + 2,             // + h: P is in shared memory (4 arrivals)
+    B_O = B_P + 2,             // + h: O += P V is done, so P's buffer is free again
+    B_END = B_O + 2,           // + h: every MMA of that head has completed
+    B_VZ = B_END + 2,          // the last V tile's rows past the keys are zero
+    NBAR
 };
 constexpr int kSmem = OFF_BAR + NBAR * 8 + 16 + 1024;  // + tmem base, abort flag, alignment slack
+static_assert(kSmem <= 232448, "shared memory per CTA");
 constexpr unsigned kFull = 0xffffffffu;
 
 struct TcParams {
@@ -66,6 +81,23 @@ __device__ __forceinline__ bool tc_warp_wait(uint32_t bar, uint32_t parity, vola
 __device__ __forceinline__ void tc_abort(int32_t *err, volatile int *abort_flag) {
     raise_err(err, PA_DEVERR_TIMEOUT);
     *abort_flag = 1;
+}
+
+// The K/V tiles go through the ring in the order the MMAs consume them:
+//   K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1)
+// (the next tile's QK is issued before the current tile's PV). Load i uses slot i % kRing.
+__device__ __forceinline__ int load_index_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int load_index_v(int j, int nkv) { return j == nkv - 1 ? 2 * nkv - 1 : 2 * j + 2; }
+__device__ __forceinline__ void load_item(int i, int nkv, int &j, bool &is_v) {
+    if (i == 0) {
+        j = 0, is_v = false;
+    } else if (i & 1) {
+        const int t = (i - 1) >> 1;
+        if (t + 1 < nkv) j = t + 1, is_v = false;
+        else j = nkv - 1, is_v = true;
+    } else {
+        j = (i - 2) >> 1, is_v = true;
+    }
 }
 
 template <class E>
@@ -119,9 +151,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
         return;
     }
+    const int last_valid = n_end - (nkv - 1) * BN;  // keys in the last tile
+    const bool zero_tail = last_valid < BN;         // its V rows past the keys must be zeroed
 
     if (tid == 0) {
-        for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), (i == B_PA || i == B_PB) ? 4 : 1);
+        for (int i = 0; i < NBAR; ++i) {
+            uint32_t count = 1;
+            if (i >= B_EMPTY && i < B_EMPTY + kRing) count = 2;
+            if (i >= B_F && i < B_O) count = 4;  // B_F, B_P
+            mbar_init(bar(i), count);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -146,228 +185,222 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         __syncwarp();
         const int R = p.box_rows, nbox = BN / R;
         const uint32_t box_bytes = static_cast<uint32_t>(R) * 128;  // one half-row box
-        int issued = 0;
-        for (int j = 0; j < nkv; ++j) {
-            const int st = j & 1;
-            const uint32_t ph = (j >> 1) & 1;
-            // this lane's box (lanes 0 .. nbox-1): its first key row, or -1 past the keys
-            const int n0 = j * BN;
-            int row = -1;
-            if (lane < nbox && n0 + lane * R < n_end) {
-                const int pos = n0 + lane * R;
-                row = trow ? trow[p.geom.block_of(pos)] * p.geom.block_size + p.geom.offset_of(pos)
-                           : k0 + pos;
-            }
-            const uint32_t nvalid_boxes = __popc(__ballot_sync(kFull, row >= 0));
-            const uint32_t bytes = nvalid_boxes * box_bytes * 2;  // both halves
-            for (int kv = 0; kv < 2; ++kv) {
-                if (!tc_warp_wait(bar((kv ? B_VE0 : B_KE0) + st), ph ^ 1, abort_flag)) {
-                    if (lane == 0) tc_abort(p.err, abort_flag);
-                    goto producer_done;
+        const int nload = 2 * nkv;
+        int issued = 0, cur_j = -1, row = -1;
+        uint32_t bytes = 0;
+        for (int i = 0; i < nload; ++i) {
+            int j;
+            bool is_v;
+            load_item(i, nkv, j, is_v);
+            if (j != cur_j) {
+                // this lane's box (lanes 0 .. nbox-1): its first key row, or -1 past the keys
+                const int n0 = j * BN;
+                row = -1;
+                if (lane < nbox && n0 + lane * R < n_end) {
+                    const int pos = n0 + lane * R;
+                    row = trow ? trow[p.geom.block_of(pos)] * p.geom.block_size + p.geom.offset_of(pos)
+                               : k0 + pos;
                 }
-                if (lane == 0) mbar_arrive_expect_tx(bar((kv ? B_VF0 : B_KF0) + st), bytes);
-                __syncwarp();
-                if (row >= 0) {
-                    const uint32_t dst = sbase + (kv ? OFF_V : OFF_K) + st * kTile + lane * R * 128;
-                    for (int half = 0; half < 2; ++half)
-                        tma_load_3d(dst + half * kHalf, kv ? &p.tm_v : &p.tm_k, half * 64, g, row,
-                                    bar((kv ? B_VF0 : B_KF0) + st));
-                }
+                bytes = __popc(__ballot_sync(kFull, row >= 0)) * box_bytes * 2;  // both halves
+                cur_j = j;
             }
-            issued = j + 1;
+            const int slot = i % kRing;
+            const uint32_t ph = (i / kRing) & 1;
+            if (!tc_warp_wait(bar(B_EMPTY + slot), ph ^ 1, abort_flag)) {
+                if (lane == 0) tc_abort(p.err, abort_flag);
+                break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL + slot), bytes);
+            __syncwarp();
+            if (row >= 0) {
+                const uint32_t dst = sbase + OFF_RING + slot * kTile + lane * R * 128;
+                for (int half = 0; half < 2; ++half)
+                    tma_load_3d(dst + half * kHalf, is_v ? &p.tm_v : &p.tm_k, half * 64, g, row,
+                                bar(B_FULL + slot));
+            }
+            issued = i + 1;
         }
-    producer_done:
-        // no copy may still be in flight at exit: the last two stages of each ring
+        // The last tile may hold rows past the keys (unwritten slots or another prompt): zero its
+        // V rows there before any PV reads them (P is zero there, but 0 * NaN is not).
+        if (issued == nload && zero_tail) {
+            const int i = nload - 1, slot = i % kRing;
+            if (tc_warp_wait(bar(B_FULL + slot), (i / kRing) & 1, abort_flag)) {
+                unsigned char *vt = smem + OFF_RING + slot * kTile;
+                for (int c = lane; c < (BN - last_valid) * 16; c += 32) {  // 16-byte chunks
+                    const int r = last_valid + c / 16, c16 = c % 16;
+                    *reinterpret_cast<uint4 *>(vt + (c16 >> 3) * kHalf + r * 128 + (c16 & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_VZ));
+            } else if (lane == 0) {
+                tc_abort(p.err, abort_flag);
+            }
+        }
+        // no copy may still be in flight at exit: the last load of every slot
         if (lane == 0) {
-            const int from = issued > 2 ? issued - 2 : 0;
-            for (int j = from; j < issued; ++j)
-                for (int kv = 0; kv < 2; ++kv)
-                    if (!mbar_wait(bar((kv ? B_VF0 : B_KF0) + (j & 1)), (j >> 1) & 1))
-                        tc_abort(p.err, abort_flag);
+            for (int i = issued > kRing ? issued - kRing : 0; i < issued; ++i)
+                if (!mbar_wait(bar(B_FULL + i % kRing), (i / kRing) & 1)) tc_abort(p.err, abort_flag);
             if (!mbar_wait(bar(B_Q), 0)) tc_abort(p.err, abort_flag);
         }
-    } else if (warp == 1) {
-        // ================================= MMA issuer =================================
+        __syncwarp();
+    } else if (warp == 1 || warp == 2) {
+        // ============================ MMA issuer of one head =============================
+        const int h = warp - 1;
         constexpr uint32_t IQK = idesc_f16(BM, BN, E::kIsBf16, false);
         constexpr uint32_t IPV = idesc_f16(BM, HD, E::kIsBf16, true);
-        auto qk = [&](int h, int st) {
-            const uint32_t d = tmem + (h ? 128 : 0);
-            const uint32_t qa = sbase + (h ? OFF_QB : OFF_QA), kb = sbase + OFF_K + st * kTile;
+        // Descriptors are built once; each MMA adds a compile-time offset (in 16-byte units) to a
+        // base. Rebuilding a descriptor from its address before every MMA halves the issue rate.
+        const uint64_t dq = smem_desc_sw128(sbase + (h ? OFF_QB : OFF_QA), 16, 1024);
+        const uint64_t dp = smem_desc_sw128(sbase + (h ? OFF_PB : OFF_PA), 16, 1024);
+        const uint64_t dk0 = smem_desc_sw128(sbase + OFF_RING, 16, 1024);
+        const uint64_t dv0 = smem_desc_sw128(sbase + OFF_RING, kHalf, 1024);
+        const uint32_t s_tm = tmem + (h ? 128 : 0), o_tm = tmem + 256 + (h ? 128 : 0);
+        auto qk = [&](int slot) {  // S = Q K^T: A = Q (K-major), B = K rows (K-major)
+            const uint64_t kb = dk0 + slot * kTileDesc;
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                tc_mma_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-                          IQK, kk > 0);
+                const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                tc_mma_ss(s_tm, dq + off, kb + off, IQK, kk > 0);
             }
         };
-        auto pv = [&](int h, int st, int j) {
-            const uint32_t d = tmem + 256 + (h ? 128 : 0);
-            const uint32_t pa = tmem + (h ? 128 : 0);
-            const uint32_t vb = sbase + OFF_V + st * kTile;
+        auto pv = [&](int slot, int j) {  // O += P V: A = P (K-major), B = V rows (N-major)
+            const uint64_t vb = dv0 + slot * kTileDesc;
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-                tc_mma_ts(d, pa + kk * 8, smem_desc_sw128(vb + kk * 2048, kHalf, 1024), IPV,
-                          (j > 0 || kk > 0));
+            for (int kk = 0; kk < BN / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                tc_mma_ss(o_tm, dp + off, vb + ((kk * 2048) >> 4), IPV, (j > 0 || kk > 0));
+            }
         };
-        bool ok = tc_warp_wait(bar(B_Q), 0, abort_flag) && tc_warp_wait(bar(B_KF0), 0, abort_flag);
+        bool ok = tc_warp_wait(bar(B_Q), 0, abort_flag) && tc_warp_wait(bar(B_FULL), 0, abort_flag);
         if (ok) {
             tc_fence_after();
             if (lane == 0) {
-                qk(0, 0);
-                tc_commit(bar(B_SA));
-                qk(1, 0);
-                tc_commit(bar(B_SB));
-                tc_commit(bar(B_KE0));
+                qk(0);
+                tc_commit(bar(B_S + h));
+                tc_commit(bar(B_EMPTY));
             }
             __syncwarp();
         }
         for (int j = 0; ok && j < nkv; ++j) {
-            const int vst = j & 1, kst = (j + 1) & 1;
-            const uint32_t vph = (j >> 1) & 1, kph = ((j + 1) >> 1) & 1;
-            ok = tc_warp_wait(bar(B_PA), j & 1, abort_flag) && tc_warp_wait(bar(B_VF0 + vst), vph, abort_flag);
+            // S(j+1) as soon as the softmax holds S(j) in registers
+            ok = tc_warp_wait(bar(B_F + h), j & 1, abort_flag);
             if (!ok) break;
-            tc_fence_after();
-            if (lane == 0) {
-                pv(0, vst, j);
-                tc_commit(bar(B_OA));
-            }
-            __syncwarp();
             if (j + 1 < nkv) {
-                ok = tc_warp_wait(bar(B_KF0 + kst), kph, abort_flag);
+                const int i = load_index_k(j + 1), slot = i % kRing;
+                ok = tc_warp_wait(bar(B_FULL + slot), (i / kRing) & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
-                    qk(0, kst);
-                    tc_commit(bar(B_SA));
+                    qk(slot);
+                    tc_commit(bar(B_S + h));
+                    tc_commit(bar(B_EMPTY + slot));
                 }
                 __syncwarp();
             }
-            ok = tc_warp_wait(bar(B_PB), j & 1, abort_flag);
+            const int i = load_index_v(j, nkv), slot = i % kRing;
+            ok = tc_warp_wait(bar(B_P + h), j & 1, abort_flag) &&
+                 tc_warp_wait(bar(B_FULL + slot), (i / kRing) & 1, abort_flag);
+            if (ok && j == nkv - 1 && zero_tail) ok = tc_warp_wait(bar(B_VZ), 0, abort_flag);
             if (!ok) break;
             tc_fence_after();
             if (lane == 0) {
-                pv(1, vst, j);
-                tc_commit(bar(B_OB));
-                tc_commit(bar(B_VE0 + vst));
-                if (j + 1 < nkv) {
-                    qk(1, kst);
-                    tc_commit(bar(B_SB));
-                    tc_commit(bar(B_KE0 + kst));
-                }
+                pv(slot, j);
+                tc_commit(bar(B_O + h));
+                tc_commit(bar(B_EMPTY + slot));
             }
             __syncwarp();
         }
         if (!ok && lane == 0) tc_abort(p.err, abort_flag);
         // every MMA this thread issued has finished before the TMEM can be freed
         if (lane == 0) {
-            tc_commit(bar(B_END));
-            if (!mbar_wait(bar(B_END), 0)) tc_abort(p.err, abort_flag);
+            tc_commit(bar(B_END + h));
+            if (!mbar_wait(bar(B_END + h), 0)) tc_abort(p.err, abort_flag);
         }
         __syncwarp();
     } else if (warp >= 4) {
         // =================================== softmax ===================================
         const int h = warp >= 8 ? 1 : 0;
         const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;                       // row of the tile = TMEM lane
+        const int r = quarter * 32 + lane;  // row of the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t srow = tmem + lane_off + (h ? 128 : 0);   // S, then P in its first 64 columns
+        const uint32_t srow = tmem + lane_off + (h ? 128 : 0);
         const uint32_t orow = tmem + lane_off + 256 + (h ? 128 : 0);
+        unsigned char *prow = smem + (h ? OFF_PB : OFF_PA) + r * 128;  // this row of P, half 0
         const int hq = h ? hB : hA;
         const int lim = p.causal ? min(kl, P + m0 + r + 1) : kl;  // keys this row may see
-        const uint32_t s_full = bar(h ? B_SB : B_SA), p_full = bar(h ? B_PB : B_PA);
-        const uint32_t o_done = bar(h ? B_OB : B_OA);
+        const uint32_t s_full = bar(B_S + h), s_free = bar(B_F + h), p_full = bar(B_P + h);
+        const uint32_t o_done = bar(B_O + h);
         float m_use = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkv; ++j) {
             if (!(ok = tc_warp_wait(s_full, j & 1, abort_flag))) break;
             tc_fence_after();
-            const int n0 = j * BN;
-            const bool masked = n0 + BN > lim;
-            uint32_t va[32], vb[32];
-            // pass 1: row maximum of the raw scores (the scale is positive, so it is applied once)
-            float ma = -INFINITY, mb2 = -INFINITY;
+            uint32_t sv[128];
 #pragma unroll
-            for (int c = 0; c < 4; c += 2) {
-                tmem_ld32(srow + c * 32, va);
-                tmem_ld32(srow + (c + 1) * 32, vb);
-                tmem_wait_ld();
-                if (masked) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        if (n0 + c * 32 + e >= lim) va[e] = 0xff800000u;        // -inf
-                        if (n0 + (c + 1) * 32 + e >= lim) vb[e] = 0xff800000u;
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    ma = fmaxf(ma, __uint_as_float(va[e]));
-                    mb2 = fmaxf(mb2, __uint_as_float(vb[e]));
-                }
+            for (int c = 0; c < 4; ++c) {
+                uint32_t(&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c);
+                tmem_ld32(srow + c * 32, chunk);
             }
-            const float mraw = fmaxf(ma, mb2);
+            tmem_wait_ld();
+            // S may be overwritten by the next tile's QK from here on
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);
+            const int n0 = j * BN;
+            if (n0 + BN > lim) {
+#pragma unroll
+                for (int e = 0; e < 128; ++e)
+                    if (n0 + e >= lim) sv[e] = 0xff800000u;  // -inf
+            }
+            // row maximum of the raw scores (the scale is positive, so it is applied once)
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int e = 0; e < 128; ++e) mq[e & 3] = fmaxf(mq[e & 3], __uint_as_float(sv[e]));
+            const float mraw = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             const float mx = mraw == -INFINITY ? -INFINITY : mraw * p.scale_log2;
             // move the reference max only when it grew by more than 2^8 (or was unset)
             const bool need = mx > m_use + 8.f;
-            if (__any_sync(kFull, need && j > 0)) {
-                if (!(ok = tc_warp_wait(o_done, (j - 1) & 1, abort_flag))) break;
-                tc_fence_after();
-                const float f = need ? fast_exp2(m_use - mx) : 1.f;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(orow + c * 32, va);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) va[e] = __float_as_uint(__uint_as_float(va[e]) * f);
-                    tmem_st32(orow + c * 32, va);
-                }
-                if (need) l *= f;
-            }
+            const float f = need ? fast_exp2(m_use - mx) : 1.f;  // 0 while m_use is unset
             if (need) m_use = mx;
             const float mu = m_use == -INFINITY ? 0.f : m_use;
-            // pass 2: p = 2^(s * scale - m) on fp32 pairs, written back as 16-bit pairs
+            // p = 2^(s * scale - m) on fp32 pairs, packed to 16-bit pairs
             const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-mu, -mu);
             uint64_t l2 = f2_pack(0.f, 0.f);
+            uint32_t pk[64];
 #pragma unroll
-            for (int c = 0; c < 4; c += 2) {
-                tmem_ld32(srow + c * 32, va);
-                tmem_ld32(srow + (c + 1) * 32, vb);
-                tmem_wait_ld();
-                uint32_t pk[2][16];
+            for (int e = 0; e < 128; e += 2) {
+                const uint64_t x2 = f2_fma(u2_pack(sv[e], sv[e + 1]), sc2, nm2);
+                const float p0 = fast_exp2(f2_lo(x2)), p1 = fast_exp2(f2_hi(x2));
+                l2 = f2_add(l2, f2_pack(p0, p1));
+                pk[e >> 1] = E::pack2(p0, p1);
+            }
+            l = l * f + (f2_lo(l2) + f2_hi(l2));
+            // P(j-1) has been consumed and O(j-1) is complete
+            if (j > 0) {
+                if (!(ok = tc_warp_wait(o_done, (j - 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                if (__any_sync(kFull, need)) {
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const uint32_t *v = half ? vb : va;
-                    const int kb = n0 + (c + half) * 32;
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(orow + c * 32, ov);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const uint64_t x2 = f2_fma(u2_pack(v[e], v[e + 1]), sc2, nm2);
-                        float x0 = f2_lo(x2), x1 = f2_hi(x2);
-                        if (masked) {
-                            if (kb + e >= lim) x0 = -INFINITY;
-                            if (kb + e + 1 >= lim) x1 = -INFINITY;
-                        }
-                        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-                        l2 = f2_add(l2, f2_pack(p0, p1));
-                        pk[half][e >> 1] = E::pack2(p0, p1);
+                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+                        tmem_st32(orow + c * 32, ov);
                     }
+                    tmem_wait_st();
                 }
-                tmem_st16(srow + c * 16, pk[0]);
-                tmem_st16(srow + (c + 1) * 16, pk[1]);
             }
-            l += f2_lo(l2) + f2_hi(l2);
-            tmem_wait_st();
-            // the last tile may hold rows past the keys (unwritten slots or another prompt):
-            // head A's warps zero those V rows before any PV reads them
-            const int valid = n_end - n0;
-            if (h == 0 && j == nkv - 1 && valid < BN) {
-                if (!(ok = tc_warp_wait(bar(B_VF0 + (j & 1)), (j >> 1) & 1, abort_flag))) break;
-                unsigned char *vt = smem + OFF_V + (j & 1) * kTile;
-                for (int i = r; i < (BN - valid) * 16; i += 128) {  // 16-byte chunks
-                    const int row = valid + i / 16, c16 = i % 16;
-                    *reinterpret_cast<uint4 *>(vt + (c16 >> 3) * kHalf + row * 128 + (c16 & 7) * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-            }
+            // P row r: 16-byte chunk q of half q / 8 sits at chunk (q % 8) ^ (r % 8) of the
+            // 128-byte row (the 128-byte swizzle the MMA descriptor names)
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                *reinterpret_cast<uint4 *>(prow + (q >> 3) * kHalf + (((q & 7) ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
