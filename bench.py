@@ -372,6 +372,8 @@ def run_gpu(args, ws_, rank, local):
     rows = {}
     if not args.skip_prefill:
         rows.update(bench_prefill(torch, pa, dev, stream, bf16_peak, hbm, args))
+    if not args.skip_small:
+        rows["decode_small_graphs"] = bench_small_decode(torch, pa, dev, hbm)
     st_mean = statistics.mean(st_ms)
     st_bytes = 4 * c0.B * c0.Hkv * c0.D * 2
     rows["store_kv_decode"] = {"kernel": "store_kv_kernel", "ms": st_mean,
@@ -420,6 +422,60 @@ def run_gpu(args, ws_, rank, local):
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def bench_small_decode(torch, pa, dev, hbm) -> dict:
+    """The two small decode workloads, whose whole KV set fits in L2: one layer-step is a few
+    microseconds, so they are timed as a CUDA graph of L independent layers (own pools and inputs),
+    L chosen so that the graph's pools exceed 4x L2 (at most 32), and reported per layer."""
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    l2 = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    res = {}
+    for name in ("tiny", "qwen25_05b_decode"):
+        base = W.CONFIGS[name].seed
+        first = W.make(name, seed=base)
+        pool_bytes = 2 * int(first.k_cache.nbytes)
+        n_layers = max(1, min(32, -(-4 * l2 // pool_bytes)))
+        layers = [DecodeLayer(torch, pa, first if l == 0 else W.make(name, seed=base + 100 + l), dev)
+                  for l in range(n_layers)]
+        kv = statistics.mean(kv_bytes(L.c.context_lens, L.c.Hkv, L.c.D) for L in layers)
+
+        def body(with_store):
+            for L in layers:
+                if with_store:
+                    pa.pa_store_kv(L.k_new, L.v_new, L.kc, L.vc, L.sm)
+                pa.pa_decode(L.out, L.q, L.kc, L.vc, L.bt, L.cl, L.c.scale, workspace=L.ws)
+
+        us = {}
+        for with_store in (True, False):
+            body(with_store)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                body(with_store)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(20):
+                a, b = ev(), ev()
+                a.record()
+                g.replay()
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            us[with_store] = statistics.median(ts) * 1e3 / n_layers
+            del g
+        c = layers[0].c
+        res[name] = {"seqs": c.B, "Hq": c.Hq, "Hkv": c.Hkv, "D": c.D, "block_size": c.block_size,
+                     "dtype": c.dtype, "kv_bytes_per_layer": int(kv), "layers_in_graph": n_layers,
+                     "us_store_plus_decode_per_layer": us[True], "us_decode_per_layer": us[False],
+                     "decode_GB_per_s": kv / (us[False] * 1e-6) / 1e9,
+                     "frac_of_hbm": kv / (us[False] * 1e-6) / 1e9 / hbm,
+                     "l2": f"{n_layers} layers x {pool_bytes / 1e6:.1f} MB of pools per graph replay"}
+        del layers
+        torch.cuda.empty_cache()
+    return res
 
 
 def bench_prefill(torch, pa, dev, stream, bf16_peak, hbm, args) -> dict:
@@ -475,6 +531,8 @@ def main():
                     choices=[k for k, w in W.CONFIGS.items() if w.kind == "decode"])
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-small", action="store_true",
+                    help="skip the CUDA-graph timing of the two small decode workloads")
     ap.add_argument("--layers", type=int, default=2, help="layers whose pools alternate")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clock-tail", action="store_true")

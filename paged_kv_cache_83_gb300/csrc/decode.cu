@@ -661,38 +661,80 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
 }
 
 // One CTA per decode CTA: if that CTA's first pair began in an earlier CTA and ends in this one,
-// combine the pair's partial segments into the output.
+// combine the pair's partial segments into the output. Every global read that the result depends
+// on is issued in parallel (records, then the segments' max and sum, then the partial rows), so the
+// kernel costs a few memory round trips whatever the number of segments.
+constexpr int kMergeMaxCtas = 512;  // decode CTAs per launch (2 per SM at most)
+
 template <int D, int G, class E>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ DecodeParams p) {
     using T = typename E::T;
-    const int c = blockIdx.x, P = gridDim.x;
+    __shared__ int seg_cta[kMergeMaxCtas];            // contributing CTAs, in CTA order
+    __shared__ unsigned char seg_slot[kMergeMaxCtas];  // which of the CTA's two partials
+    __shared__ float seg_m[kMergeMaxCtas][G];          // segment max (log2 domain), then weight
+    __shared__ float seg_l[kMergeMaxCtas][G];          // segment sum
+    __shared__ float norm[G];
+    __shared__ int nseg_s;
+    const int c = blockIdx.x, P = gridDim.x, tid = threadIdx.x, lane = tid & 31;
     const SegRecord rc = p.rec[c];
     if (rc.b < 0 || rc.pair_start >= rc.lo || rc.pair_start + rc.ntiles > rc.hi) return;
     // first CTA whose range holds the pair's first tile: max{c' : lo(c') <= pair_start}
     const long long x = rc.pair_start;
     int c0 = static_cast<int>(((x + 1) * P + rc.total - 1) / rc.total) - 1;
     if (c0 < 0) c0 = 0;
-    const size_t bh = static_cast<size_t>(rc.b) * p.Hq + static_cast<size_t>(rc.g) * G;
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int h = idx / D, d = idx % D;
+    if (tid < 32) {  // the CTAs in [c0, c] that hold tiles (ranges can be empty when tiles < CTAs)
+        int n = 0;
+        for (int base = c0; base <= c; base += 32) {
+            const int cc = base + lane;
+            bool has = false;
+            int slot = 0;
+            if (cc <= c) {
+                const SegRecord r = p.rec[cc];
+                has = r.lo < r.hi;
+                slot = (cc == c0 && r.lo < x) ? 1 : 0;
+            }
+            const unsigned m = __ballot_sync(kFull, has);
+            if (has) {
+                const int pos = n + __popc(m & ((1u << lane) - 1u));
+                seg_cta[pos] = cc;
+                seg_slot[pos] = static_cast<unsigned char>(slot);
+            }
+            n += __popc(m);
+        }
+        if (lane == 0) nseg_s = n;
+    }
+    __syncthreads();
+    const int nseg = nseg_s;
+    auto partial = [&](int k, int h) {
+        return p.part + ((static_cast<size_t>(seg_cta[k]) * 2 + seg_slot[k]) * G + h) * (D + 2);
+    };
+    for (int i = tid; i < nseg * G; i += blockDim.x) {
+        const int k = i / G, h = i % G;
+        const float *pp = partial(k, h);
+        seg_m[k][h] = pp[D];
+        seg_l[k][h] = pp[D + 1];
+    }
+    __syncthreads();
+    if (tid < G) {  // reference max, segment weights and the normaliser, segments in order
+        const int h = tid;
         float M = -INFINITY;
-        for (int cc = c0; cc <= c; ++cc) {
-            const SegRecord r = p.rec[cc];
-            if (r.lo >= r.hi) continue;
-            const int slot = (cc == c0 && r.lo < x) ? 1 : 0;
-            M = fmaxf(M, p.part[((static_cast<size_t>(cc) * 2 + slot) * G + h) * (D + 2) + D]);
-        }
+        for (int k = 0; k < nseg; ++k) M = fmaxf(M, seg_m[k][h]);
         const float mu = M == -INFINITY ? 0.f : M;
-        float L = 0.f, O = 0.f;
-        for (int cc = c0; cc <= c; ++cc) {
-            const SegRecord r = p.rec[cc];
-            if (r.lo >= r.hi) continue;
-            const int slot = (cc == c0 && r.lo < x) ? 1 : 0;
-            const float *pp = p.part + ((static_cast<size_t>(cc) * 2 + slot) * G + h) * (D + 2);
-            const float w = pp[D + 1] * fast_exp2(pp[D] - mu);
+        float L = 0.f;
+        for (int k = 0; k < nseg; ++k) {
+            const float w = seg_l[k][h] * fast_exp2(seg_m[k][h] - mu);
+            seg_m[k][h] = w;
             L += w;
-            O = fmaf(w, pp[d], O);
         }
+        norm[h] = L;
+    }
+    __syncthreads();
+    const size_t bh = static_cast<size_t>(rc.b) * p.Hq + static_cast<size_t>(rc.g) * G;
+    for (int idx = tid; idx < G * D; idx += blockDim.x) {
+        const int h = idx / D, d = idx % D;
+        float O = 0.f;
+        for (int k = 0; k < nseg; ++k) O = fmaf(seg_m[k][h], partial(k, h)[d], O);
+        const float L = norm[h];
         static_cast<T *>(p.out)[(bh + h) * D + d] = T(L > 0.f ? O / L : 0.f);
     }
 }
@@ -752,6 +794,7 @@ cudaError_t launch_typed(DecodeParams &prm, cudaStream_t stream) {
         configured[dev] = smem;
     }
     const int P = device_sm_count() * ctas_per_sm<G>();
+    if (P > kMergeMaxCtas) return cudaErrorInvalidConfiguration;
     kern<<<P, kThreads, smem, stream>>>(prm);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
