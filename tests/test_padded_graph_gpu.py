@@ -1,0 +1,76 @@
+"""Decode batches padded to a fixed size and replayed from one captured CUDA graph.
+
+An engine captures one graph per batch-size bucket and fills unused rows with padding (nano-vLLM
+Part 4 §3 on CUDA graphs per batch size; smzdm deep dive "GPU执行优化"). A padding row has
+context length 0, slot -1 and a table row of -1: the store skips it, the decode writes zeros for
+it, and it costs no KV traffic. The graph of store + decode is captured once for a 64-row bucket
+and replayed after different real batches (40, 64 and 1 rows) are copied into its input buffers.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_83_gb300 as pa
+import workloads as W
+from tests.gpu_util import TOL, bits, err_buf, f64, i32, max_abs, to_dev, workspace
+
+pytestmark = pytest.mark.gpu
+
+BUCKET, NB, BS, MAXB = 64, 4096, 16, 64  # 64 rows x 64 blocks fit the pool
+Hq, Hkv, D, DT = 16, 8, 128, "bf16"
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.get()
+
+
+def _batch(n_real, seed):
+    rng = np.random.default_rng([seed, 5])
+    ctx = np.zeros(BUCKET, np.int64)
+    ctx[:n_real] = rng.integers(1, MAXB * BS, size=n_real)
+    return W.decode_case(B=BUCKET, Hq=Hq, Hkv=Hkv, D=D, block_size=BS, dtype=DT, context_lens=ctx,
+                         num_blocks=NB, max_blocks_per_seq=MAXB, seed=seed)
+
+
+def test_padded_bucket_graph_replays(orc):
+    c0 = _batch(BUCKET, 1)
+    bufs = {"q": to_dev(c0.q, DT), "kn": to_dev(c0.k_new, DT), "vn": to_dev(c0.v_new, DT),
+            "kc": to_dev(c0.k_cache, DT), "vc": to_dev(c0.v_cache, DT),
+            "bt": i32(c0.block_tables), "cl": i32(c0.context_lens), "sm": i32(c0.slot_mapping)}
+    out = torch.empty_like(bufs["q"])
+    ws = workspace(BUCKET, Hq, Hkv, D, MAXB, BS)
+    err = err_buf()
+
+    def body():
+        pa.pa_store_kv(bufs["kn"], bufs["vn"], bufs["kc"], bufs["vc"], bufs["sm"], err=err)
+        pa.pa_decode(out, bufs["q"], bufs["kc"], bufs["vc"], bufs["bt"], bufs["cl"], c0.scale,
+                     workspace=ws, err=err)
+
+    body()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        body()
+
+    for n_real, seed in [(40, 2), (BUCKET, 3), (1, 4), (40, 2)]:
+        c = _batch(n_real, seed)
+        src = {"q": c.q, "kn": c.k_new, "vn": c.v_new, "kc": c.k_cache, "vc": c.v_cache}
+        for key, a in src.items():
+            bufs[key].copy_(to_dev(a, DT))
+        for key, a in (("bt", c.block_tables), ("cl", c.context_lens), ("sm", c.slot_mapping)):
+            bufs[key].copy_(i32(a))
+        out.fill_(float("nan"))
+        err.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        kref, vref = orc.store_kv(c.k_new, c.v_new, c.k_cache, c.v_cache, c.slot_mapping)
+        assert np.array_equal(bits(bufs["kc"]), kref) and np.array_equal(bits(bufs["vc"]), vref)
+        o = f64(out)
+        ref = orc.decode(c.q[:n_real], kref, vref, c.block_tables[:n_real],
+                         c.context_lens[:n_real], scale=c.scale, dtype=DT)
+        e = max_abs(o[:n_real], ref)
+        assert e <= TOL[DT], (n_real, e)
+        assert np.all(o[n_real:] == 0.0), n_real  # padding rows: zeros, not stale values

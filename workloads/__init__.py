@@ -189,7 +189,7 @@ class PrefillCase:
     block_size: int
     num_blocks: int
     scale: float
-    prefix_len: int
+    prefix_len: int            # -1: a prefix length per sequence (k_lens - q_lens)
     q: np.ndarray              # uint16 [Tq, Hq, D]
     k: np.ndarray              # uint16 [Tq, Hkv, D]  new tokens only
     v: np.ndarray
@@ -276,7 +276,7 @@ def decode_case(*, B: int, Hq: int, Hkv: int, D: int, block_size: int, dtype: st
                       context_lens=ctx.astype(np.int32), slot_mapping=slots, seed=seed)
 
 
-def prefill_case(*, q_lens, prefix_len: int, Hq: int, Hkv: int, D: int, block_size: int,
+def prefill_case(*, q_lens, prefix_len, Hq: int, Hkv: int, D: int, block_size: int,
                  dtype: str, pool_factor: float = 1.25, num_blocks: int | None = None,
                  shared_prefix: bool = True, seed: int = 0, name: str = "custom") -> PrefillCase:
     """Build a prefill step over packed prompts.
@@ -285,15 +285,24 @@ def prefill_case(*, q_lens, prefix_len: int, Hq: int, Hkv: int, D: int, block_si
     new tokens. With ``shared_prefix`` the prefix must be whole blocks and all sequences point
     at the same prefix blocks (one allocation, its refcount raised once per extra sharer), the
     way a prefix cache reuses full blocks of a common system prompt. The new tokens' slots
-    follow the prefix in each sequence's own blocks.
+    follow the prefix in each sequence's own blocks. ``prefix_len`` may also be one length per
+    sequence (private prefixes): a sequence with one new token and a prefix of n - 1 is a decode
+    row of a mixed prefill + decode batch.
     """
     rng = np.random.default_rng([seed, 1])
     ql = np.asarray(q_lens, dtype=np.int64)
     S = int(ql.shape[0])
-    P = int(prefix_len)
+    per_seq = np.ndim(prefix_len) > 0
+    Ps = (np.asarray(prefix_len, dtype=np.int64) if per_seq
+          else np.full(S, int(prefix_len), dtype=np.int64))
+    if Ps.shape != (S,) or (Ps < 0).any():
+        raise ValueError("prefix_len: one non-negative length, or one per sequence")
+    if per_seq:
+        shared_prefix = False
+    P = -1 if per_seq else int(prefix_len)
     if shared_prefix and P % block_size:
         raise ValueError("a shared prefix must be a whole number of blocks")
-    kl = ql + P
+    kl = ql + Ps
     nblk = [(int(k) + block_size - 1) // block_size for k in kl]
     npre = P // block_size if shared_prefix else 0
     total = (npre + sum(n - npre for n in nblk)) if shared_prefix else sum(nblk)
@@ -319,7 +328,7 @@ def prefill_case(*, q_lens, prefix_len: int, Hq: int, Hkv: int, D: int, block_si
     slots = np.empty(Tq, dtype=np.int32)
     for s in range(S):
         for r in range(int(ql[s])):
-            slots[cu_q[s] + r] = _slot(bt[s], P + r, block_size)
+            slots[cu_q[s] + r] = _slot(bt[s], int(Ps[s]) + r, block_size)
 
     q = normal_bits(Tq * Hq * D, dtype, seed, 20).reshape(Tq, Hq, D)
     k = normal_bits(Tq * Hkv * D, dtype, seed, 21).reshape(Tq, Hkv, D)
