@@ -6,29 +6,35 @@
 // boundaries) and "模型实现细节" (prefix cache used when cu_seqlens_k > cu_seqlens_q); "mini-vLLM"
 // (prompts attending causally to themselves).
 //
-// One CTA computes 128 query rows of one sequence for two query heads that share a kv head (a
-// GQA pair), so every K/V tile it loads serves 256 rows. Shapes: head dim 128, even group sizes.
+// Persistent: one CTA per SM takes work items (128 query rows of one sequence for the two query
+// heads of a GQA pair, which share every K/V tile) from a counter until none is left, so the
+// start-up of one item overlaps the end of the previous one. Shapes: head dim 128, even groups.
 //
-//   warp 0      producer: TMA loads of the two Q tiles, then of 128-key K and V tiles through the
-//               block table (or from the packed k, v), 128-byte swizzled, into a 3-slot ring in
-//               the order the MMAs consume them (K0, K1, V0, K2, V1, ...).
+//   warp 3      scheduler: claims items, reads their lengths, checks the block table, drops items
+//               without rows, writes zero rows + an error bit for bad ones, and queues the rest.
+//   warp 0      producer: TMA loads of each item's two Q tiles and of 128-key K and V tiles
+//               through the block table (or from the packed k, v), 128-byte swizzled, into a
+//               3-slot ring in the order the MMAs consume them (K0, K1, V0, K2, V1, ...).
 //   warps 1, 2  one MMA issuer per head (one thread each; warp 1 owns the 512 TMEM columns):
 //                 S_h = Q_h K^T   as soon as the softmax has read S_h of the previous tile,
 //                 O_h += P_h V    as soon as P_h is in shared memory.
-//               Both operands of both MMAs come from shared memory, so S of the next tile is
-//               computed while the softmax still works on the current one.
+//               Both operands of both MMAs come from shared memory, so S of the next tile (or the
+//               next item's first tile) is computed while the softmax still works on the current one.
 //   warps 4-7   softmax of head A, warps 8-11 softmax of head B: thread = one query row = one
 //               TMEM lane. S is read once into registers (then released), masked (causal bound
 //               P + row, context end), row max, P = 2^(s - m) in bf16/fp16 stored to shared
 //               memory in the swizzled layout the PV MMA reads. O is rescaled in TMEM only when
 //               the row max grew by more than 2^8 (the normaliser uses the same reference, so the
-//               result is exact).
+//               result is exact). The output rows leave through the warp's rows of the P buffer
+//               as whole 256-byte rows.
 //   TMEM columns: S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511.
 // Every wait is bounded (PA_DEVERR_TIMEOUT); on a timeout every role drains what it started
 // (TMA, MMAs) before the TMEM is freed.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
+
+#include <atomic>
 
 #include "pa_internal.h"
 
@@ -46,18 +52,31 @@ constexpr int OFF_QA = 0, OFF_QB = kTile, OFF_PA = 2 * kTile, OFF_PB = 3 * kTile
               OFF_BAR = OFF_RING + kRing * kTile;
 // per-head barriers take index base + h (h = 0 for head A, 1 for head B)
 enum {
-    B_Q = 0,
-    B_FULL = 1,                // + slot: a K/V tile landed (TMA transaction count)
+    B_QFULL = 0,               // the item's two Q tiles landed (TMA transaction count)
+    B_QEMPTY,                  // both heads issued the item's last QK (two commits)
+    B_FULL,                    // + slot: a K/V tile landed
     B_EMPTY = B_FULL + kRing,  // + slot: both heads' MMAs are done with it (two commits)
     B_S = B_EMPTY + kRing,     // + h: S = Q K^T is in TMEM
     B_F = B_S + 2,             // + h: the softmax warps have read S (4 arrivals)
     B_P = B_F + 2,             // + h: P is in shared memory (4 arrivals)
     B_O = B_P + 2,             // + h: O += P V is done, so P's buffer is free again
-    B_END = B_O + 2,           // + h: every MMA of that head has completed
+    B_OFREE = B_O + 2,         // + h: the item's output has been read out of TMEM (4 arrivals)
+    B_END = B_OFREE + 2,       // + h: every MMA of that head has completed
     B_VZ = B_END + 2,          // the last V tile's rows past the keys are zero
-    NBAR
+    B_IFULL = B_VZ + 1,        // + k: work item k of the queue is published
+    B_IEMPTY = B_IFULL + 2,    // + k: every role has read it (kItemReaders arrivals)
+    NBAR = B_IEMPTY + 2
 };
-constexpr int kSmem = OFF_BAR + NBAR * 8 + 16 + 1024;  // + tmem base, abort flag, alignment slack
+constexpr int kItemReaders = 11;  // producer, two MMA issuers, eight softmax warps
+
+// One work item: 128 query rows of sequence s for the query heads 2 pair, 2 pair + 1.
+// nkv == 0 marks the end of the work.
+struct ItemInfo {
+    int s, q0, k0, kl, m0, mrows, P, n_end, nkv, pair, pad0, pad1;
+};
+constexpr int OFF_ITEMS = OFF_BAR + NBAR * 8;
+constexpr int OFF_MISC = OFF_ITEMS + 2 * static_cast<int>(sizeof(ItemInfo));  // tmem base, abort flag
+constexpr int kSmem = OFF_MISC + 16 + 1024;                                   // + alignment slack
 static_assert(kSmem <= 232448, "shared memory per CTA");
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -66,7 +85,9 @@ struct TcParams {
     const int32_t *cu_q, *cu_k, *block_tables;
     void *out;
     int32_t *err;
-    int S, Hq, Hkv, G, max_blocks, num_blocks, causal, max_seqlen_q, box_rows;
+    unsigned long long *sched;  // [0]: next work item, [1]: CTAs finished (both 0 between launches)
+    long long n_items;          // S * pairs * row blocks
+    int S, Hq, Hkv, G, max_blocks, num_blocks, causal, max_seqlen_q, box_rows, row_blocks, pairs;
     BlockGeom geom;
     float scale_log2;
 };
@@ -83,23 +104,12 @@ __device__ __forceinline__ void tc_abort(int32_t *err, volatile int *abort_flag)
     *abort_flag = 1;
 }
 
-// The K/V tiles go through the ring in the order the MMAs consume them:
-//   K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1)
-// (the next tile's QK is issued before the current tile's PV). Load i uses slot i % kRing.
-__device__ __forceinline__ int load_index_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
-__device__ __forceinline__ int load_index_v(int j, int nkv) { return j == nkv - 1 ? 2 * nkv - 1 : 2 * j + 2; }
-__device__ __forceinline__ void load_item(int i, int nkv, int &j, bool &is_v) {
-    if (i == 0) {
-        j = 0, is_v = false;
-    } else if (i & 1) {
-        const int t = (i - 1) >> 1;
-        if (t + 1 < nkv) j = t + 1, is_v = false;
-        else j = nkv - 1, is_v = true;
-    } else {
-        j = (i - 2) >> 1, is_v = true;
-    }
-}
-
+// Persistent: one CTA per SM takes work items from a counter until none is left.
+//
+// The K/V tiles of all the CTA's items go through the ring in the order the MMAs consume them:
+// the next tile's QK is issued before the current tile's PV, across item boundaries too:
+//   K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), K0', V(n-1), K1', V0', ...
+// Load i uses slot i % kRing; the producer and both MMA issuers count loads the same way.
 template <class E>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
     using T = typename E::T;
@@ -107,58 +117,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_addr(smem);
     const uint32_t bar0 = sbase + OFF_BAR;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_BAR + NBAR * 8);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_BAR + NBAR * 8 + 4);
+    ItemInfo *items = reinterpret_cast<ItemInfo *>(smem + OFF_ITEMS);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
     auto bar = [&](int i) { return bar0 + 8u * i; };
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int mb = gridDim.x - 1 - blockIdx.x;  // row blocks with the most keys first
-    const int pair = blockIdx.y, s = blockIdx.z;
-    const int hA = 2 * pair, hB = 2 * pair + 1, g = hA / p.G;
-
-    const int q0 = p.cu_q[s], ql = p.cu_q[s + 1] - q0;
-    const int k0 = p.cu_k[s], kl = p.cu_k[s + 1] - k0;
-    if (ql < 0 || ql > p.max_seqlen_q) {
-        if (mb == 0 && pair == 0 && tid == 0) raise_err(p.err, PA_DEVERR_LENGTH);
-        return;
-    }
-    const int m0 = mb * BM;
-    if (m0 >= ql) return;
-    const int mrows = min(BM, ql - m0);
     T *out = static_cast<T *>(p.out);
-    const int32_t *trow =
-        p.block_tables ? p.block_tables + static_cast<size_t>(s) * p.max_blocks : nullptr;
-    bool bad = kl < ql;
-    if (trow && static_cast<long long>(kl) > static_cast<long long>(p.max_blocks) * p.geom.block_size)
-        bad = true;
-    const int P = kl - ql;
-    const int n_end = bad ? 0 : (p.causal ? min(kl, P + m0 + mrows) : kl);
-    const int nkv = (n_end + BN - 1) / BN;
-    int table_bad = 0;
-    if (!bad && trow) {
-        const int nblk = p.geom.block_of(n_end - 1) + 1;
-        for (int i = tid; i < nblk; i += kThreads) {
-            const int id = trow[i];
-            if (id < 0 || id >= p.num_blocks) table_bad = 1;
-        }
-    }
-    table_bad = __syncthreads_or(table_bad);
-    if (bad || table_bad) {  // the item is skipped: its rows are zero
-        if (tid == 0) raise_err(p.err, bad ? PA_DEVERR_LENGTH : PA_DEVERR_TABLE);
-        for (int i = tid; i < mrows * HD * 2; i += kThreads) {
-            const int r = i / (2 * HD), h = (i / HD) & 1, d = i % HD;
-            out[(static_cast<size_t>(q0 + m0 + r) * p.Hq + (h ? hB : hA)) * HD + d] = T(0.f);
-        }
-        return;
-    }
-    const int last_valid = n_end - (nkv - 1) * BN;  // keys in the last tile
-    const bool zero_tail = last_valid < BN;         // its V rows past the keys must be zeroed
 
     if (tid == 0) {
         for (int i = 0; i < NBAR; ++i) {
             uint32_t count = 1;
-            if (i >= B_EMPTY && i < B_EMPTY + kRing) count = 2;
-            if (i >= B_F && i < B_O) count = 4;  // B_F, B_P
+            if (i == B_QEMPTY || (i >= B_EMPTY && i < B_EMPTY + kRing)) count = 2;
+            if ((i >= B_F && i < B_O) || (i >= B_OFREE && i < B_END)) count = 4;  // B_F, B_P, B_OFREE
+            if (i >= B_IEMPTY) count = kItemReaders;
             mbar_init(bar(i), count);
         }
         *abort_flag = 0;
@@ -170,79 +141,154 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
+    // every role reads the work items in the same order: item n sits in queue entry n % 2
+    auto read_item = [&](int n, ItemInfo &it) -> bool {
+        if (!tc_warp_wait(bar(B_IFULL + (n & 1)), (n >> 1) & 1, abort_flag)) return false;
+        it = items[n & 1];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_IEMPTY + (n & 1)));
+        return true;
+    };
+
+    if (warp == 3) {
+        // ================================== scheduler ==================================
+        // Resolves items ahead of the other roles: lengths, table check; items that cover no
+        // query rows are dropped, items with bad inputs get zero rows and an error bit.
+        int published = 0;
+        bool ok = true;
+        unsigned long long nxt = lane == 0 ? atomicAdd(p.sched, 1ull) : 0ull;
+        while (ok) {
+            const long long idx = static_cast<long long>(__shfl_sync(kFull, nxt, 0));
+            if (idx >= p.n_items) break;
+            if (lane == 0) nxt = atomicAdd(p.sched, 1ull);  // in flight while this one is resolved
+            const long long per_seq = static_cast<long long>(p.pairs) * p.row_blocks;
+            const int s = static_cast<int>(idx / per_seq);
+            const int rem = static_cast<int>(idx % per_seq);
+            const int pair = rem / p.row_blocks;
+            const int mb = p.row_blocks - 1 - rem % p.row_blocks;  // most keys first
+            const int q0 = p.cu_q[s], ql = p.cu_q[s + 1] - q0;
+            const int k0 = p.cu_k[s], kl = p.cu_k[s + 1] - k0;
+            if (ql < 0 || ql > p.max_seqlen_q) {
+                if (mb == 0 && pair == 0 && lane == 0) raise_err(p.err, PA_DEVERR_LENGTH);
+                continue;
+            }
+            const int m0 = mb * BM;
+            if (m0 >= ql) continue;
+            const int mrows = min(BM, ql - m0);
+            const int32_t *trow =
+                p.block_tables ? p.block_tables + static_cast<size_t>(s) * p.max_blocks : nullptr;
+            bool bad = kl < ql;
+            if (trow && static_cast<long long>(kl) > static_cast<long long>(p.max_blocks) * p.geom.block_size)
+                bad = true;
+            const int P = kl - ql;
+            const int n_end = bad ? 0 : (p.causal ? min(kl, P + m0 + mrows) : kl);
+            int table_bad = 0;
+            if (!bad && trow) {
+                const int nblk = p.geom.block_of(n_end - 1) + 1;
+                for (int i = lane; i < nblk; i += 32) {
+                    const int id = trow[i];
+                    if (id < 0 || id >= p.num_blocks) table_bad = 1;
+                }
+            }
+            table_bad = __any_sync(kFull, table_bad);
+            if (bad || table_bad) {  // the item is skipped: its rows are zero
+                if (lane == 0) raise_err(p.err, bad ? PA_DEVERR_LENGTH : PA_DEVERR_TABLE);
+                for (int i = lane; i < mrows * HD * 2; i += 32) {
+                    const int r = i / (2 * HD), h = (i / HD) & 1, d = i % HD;
+                    out[(static_cast<size_t>(q0 + m0 + r) * p.Hq + 2 * pair + h) * HD + d] = T(0.f);
+                }
+                continue;
+            }
+            if (!(ok = tc_warp_wait(bar(B_IEMPTY + (published & 1)), ((published >> 1) & 1) ^ 1, abort_flag)))
+                break;
+            if (lane == 0) {
+                ItemInfo it;
+                it.s = s, it.q0 = q0, it.k0 = k0, it.kl = kl, it.m0 = m0, it.mrows = mrows, it.P = P;
+                it.n_end = n_end, it.nkv = (n_end + BN - 1) / BN, it.pair = pair, it.pad0 = it.pad1 = 0;
+                items[published & 1] = it;
+                mbar_arrive(bar(B_IFULL + (published & 1)));  // release: the entry is visible
+            }
+            __syncwarp();
+            ++published;
+        }
+        // the end marker
+        if (ok && (ok = tc_warp_wait(bar(B_IEMPTY + (published & 1)), ((published >> 1) & 1) ^ 1, abort_flag))) {
+            if (lane == 0) {
+                ItemInfo it{};
+                items[published & 1] = it;
+                mbar_arrive(bar(B_IFULL + (published & 1)));
+            }
+            __syncwarp();
+        }
+        if (!ok && lane == 0) tc_abort(p.err, abort_flag);
+    } else if (warp == 0) {
         // =================================== producer ===================================
         prefetch_tmap(&p.tm_q);
         prefetch_tmap(&p.tm_k);
         prefetch_tmap(&p.tm_v);
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar(B_Q), 2 * kTile);
-            for (int h = 0; h < 2; ++h)
-                for (int half = 0; half < 2; ++half)
-                    tma_load_3d(sbase + (h ? OFF_QB : OFF_QA) + half * kHalf, &p.tm_q, half * 64,
-                                h ? hB : hA, q0 + m0, bar(B_Q));
-        }
-        __syncwarp();
         const int R = p.box_rows, nbox = BN / R;
         const uint32_t box_bytes = static_cast<uint32_t>(R) * 128;  // one half-row box
-        const int nload = 2 * nkv;
-        int issued = 0, cur_j = -1, row = -1;
-        uint32_t bytes = 0;
-        for (int i = 0; i < nload; ++i) {
-            int j;
-            bool is_v;
-            load_item(i, nkv, j, is_v);
-            if (j != cur_j) {
-                // this lane's box (lanes 0 .. nbox-1): its first key row, or -1 past the keys
-                const int n0 = j * BN;
-                row = -1;
-                if (lane < nbox && n0 + lane * R < n_end) {
-                    const int pos = n0 + lane * R;
-                    row = trow ? trow[p.geom.block_of(pos)] * p.geom.block_size + p.geom.offset_of(pos)
-                               : k0 + pos;
-                }
-                bytes = __popc(__ballot_sync(kFull, row >= 0)) * box_bytes * 2;  // both halves
-                cur_j = j;
+        long long L = 0;                                            // loads issued
+        int n = 0;                                                  // items taken
+        bool ok = true;
+        // tile j of item `it` (K or V) into the next ring slot
+        auto load_tile = [&](const ItemInfo &it, int j, bool is_v) -> bool {
+            const int32_t *trow =
+                p.block_tables ? p.block_tables + static_cast<size_t>(it.s) * p.max_blocks : nullptr;
+            const int n0 = j * BN;
+            int row = -1;  // this lane's box (lanes 0 .. nbox-1): its first key row, or -1
+            if (lane < nbox && n0 + lane * R < it.n_end) {
+                const int pos = n0 + lane * R;
+                row = trow ? trow[p.geom.block_of(pos)] * p.geom.block_size + p.geom.offset_of(pos)
+                           : it.k0 + pos;
             }
-            const int slot = i % kRing;
-            const uint32_t ph = (i / kRing) & 1;
-            if (!tc_warp_wait(bar(B_EMPTY + slot), ph ^ 1, abort_flag)) {
-                if (lane == 0) tc_abort(p.err, abort_flag);
-                break;
-            }
+            const uint32_t bytes = __popc(__ballot_sync(kFull, row >= 0)) * box_bytes * 2;
+            const int slot = static_cast<int>(L % kRing);
+            if (!tc_warp_wait(bar(B_EMPTY + slot), static_cast<uint32_t>((L / kRing) & 1) ^ 1, abort_flag))
+                return false;
             if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL + slot), bytes);
             __syncwarp();
             if (row >= 0) {
                 const uint32_t dst = sbase + OFF_RING + slot * kTile + lane * R * 128;
+                const int g = 2 * it.pair / p.G;
                 for (int half = 0; half < 2; ++half)
                     tma_load_3d(dst + half * kHalf, is_v ? &p.tm_v : &p.tm_k, half * 64, g, row,
                                 bar(B_FULL + slot));
             }
-            issued = i + 1;
-        }
-        // The last tile may hold rows past the keys (unwritten slots or another prompt): zero its
-        // V rows there before any PV reads them (P is zero there, but 0 * NaN is not).
-        if (issued == nload && zero_tail) {
-            const int i = nload - 1, slot = i % kRing;
-            if (tc_warp_wait(bar(B_FULL + slot), (i / kRing) & 1, abort_flag)) {
-                unsigned char *vt = smem + OFF_RING + slot * kTile;
-                for (int c = lane; c < (BN - last_valid) * 16; c += 32) {  // 16-byte chunks
-                    const int r = last_valid + c / 16, c16 = c % 16;
-                    *reinterpret_cast<uint4 *>(vt + (c16 >> 3) * kHalf + r * 128 + (c16 & 7) * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_VZ));
-            } else if (lane == 0) {
-                tc_abort(p.err, abort_flag);
+            ++L;
+            return true;
+        };
+        ItemInfo prev{}, cur{};
+        bool have_prev = false;
+        while (ok) {
+            if (!(ok = read_item(n, cur)) || cur.nkv == 0) break;
+            ok = load_tile(cur, 0, false);
+            if (ok && have_prev) ok = load_tile(prev, prev.nkv - 1, true);
+            // this item's Q once both heads issued the previous item's last QK
+            if (ok && n > 0) ok = tc_warp_wait(bar(B_QEMPTY), (n - 1) & 1, abort_flag);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(B_QFULL), 2 * kTile);
+                for (int h = 0; h < 2; ++h)
+                    for (int half = 0; half < 2; ++half)
+                        tma_load_3d(sbase + (h ? OFF_QB : OFF_QA) + half * kHalf, &p.tm_q, half * 64,
+                                    2 * cur.pair + h, cur.q0 + cur.m0, bar(B_QFULL));
             }
+            __syncwarp();
+            for (int j = 1; ok && j < cur.nkv; ++j)
+                ok = load_tile(cur, j, false) && load_tile(cur, j - 1, true);
+            prev = cur;
+            have_prev = true;
+            ++n;
         }
-        // no copy may still be in flight at exit: the last load of every slot
+        if (ok && have_prev) ok = load_tile(prev, prev.nkv - 1, true);
+        if (!ok && lane == 0) tc_abort(p.err, abort_flag);
+        // no copy may still be in flight at exit: the last load of every slot, the last Q
         if (lane == 0) {
-            for (int i = issued > kRing ? issued - kRing : 0; i < issued; ++i)
-                if (!mbar_wait(bar(B_FULL + i % kRing), (i / kRing) & 1)) tc_abort(p.err, abort_flag);
-            if (!mbar_wait(bar(B_Q), 0)) tc_abort(p.err, abort_flag);
+            for (long long i = L > kRing ? L - kRing : 0; i < L; ++i)
+                if (!mbar_wait(bar(B_FULL + static_cast<int>(i % kRing)), static_cast<uint32_t>((i / kRing) & 1)))
+                    tc_abort(p.err, abort_flag);
+            if (n > 0 && !mbar_wait(bar(B_QFULL), (n - 1) & 1)) tc_abort(p.err, abort_flag);
         }
         __syncwarp();
     } else if (warp == 1 || warp == 2) {
@@ -265,52 +311,105 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 tc_mma_ss(s_tm, dq + off, kb + off, IQK, kk > 0);
             }
         };
-        auto pv = [&](int slot, int j) {  // O += P V: A = P (K-major), B = V rows (N-major)
+        auto pv = [&](int slot, bool acc) {  // O += P V: A = P (K-major), B = V rows (N-major)
             const uint64_t vb = dv0 + slot * kTileDesc;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                tc_mma_ss(o_tm, dp + off, vb + ((kk * 2048) >> 4), IPV, (j > 0 || kk > 0));
+                tc_mma_ss(o_tm, dp + off, vb + ((kk * 2048) >> 4), IPV, (acc || kk > 0));
             }
         };
-        bool ok = tc_warp_wait(bar(B_Q), 0, abort_flag) && tc_warp_wait(bar(B_FULL), 0, abort_flag);
-        if (ok) {
+        long long ci = 0;  // loads consumed
+        auto next_load = [&](int &slot) -> bool {
+            slot = static_cast<int>(ci % kRing);
+            const bool r = tc_warp_wait(bar(B_FULL + slot), static_cast<uint32_t>((ci / kRing) & 1), abort_flag);
+            ++ci;
+            return r;
+        };
+        // QK of the first tile of the item read as number `n`
+        auto first_qk = [&](const ItemInfo &it, int n) -> bool {
+            int slot;
+            if (!tc_warp_wait(bar(B_QFULL), n & 1, abort_flag) || !next_load(slot)) return false;
             tc_fence_after();
             if (lane == 0) {
-                qk(0);
+                qk(slot);
                 tc_commit(bar(B_S + h));
-                tc_commit(bar(B_EMPTY));
+                tc_commit(bar(B_EMPTY + slot));
+                if (it.nkv == 1) tc_commit(bar(B_QEMPTY));
             }
             __syncwarp();
-        }
-        for (int j = 0; ok && j < nkv; ++j) {
-            // S(j+1) as soon as the softmax holds S(j) in registers
-            ok = tc_warp_wait(bar(B_F + h), j & 1, abort_flag);
-            if (!ok) break;
-            if (j + 1 < nkv) {
-                const int i = load_index_k(j + 1), slot = i % kRing;
-                ok = tc_warp_wait(bar(B_FULL + slot), (i / kRing) & 1, abort_flag);
-                if (!ok) break;
+            return true;
+        };
+        int n = 0, zt = 0;  // items read, zero-tail items finished
+        long long t = 0;    // tiles of this head so far (global over the CTA's items)
+        ItemInfo cur{}, nxt{};
+        bool ok = read_item(0, cur);
+        const bool active = ok && cur.nkv > 0;  // the CTA got at least one item
+        n = 1;
+        int item_no = 0;  // index of `cur` among the CTA's items
+        if (active) ok = first_qk(cur, 0);
+        int j = 0;
+        while (ok && active) {
+            // S(t + 1) as soon as the softmax holds S(t) in registers
+            if (!(ok = tc_warp_wait(bar(B_F + h), static_cast<uint32_t>(t & 1), abort_flag))) break;
+            bool has_next = true;
+            if (j + 1 < cur.nkv) {
+                int slot;
+                if (!(ok = next_load(slot))) break;
                 tc_fence_after();
                 if (lane == 0) {
                     qk(slot);
                     tc_commit(bar(B_S + h));
                     tc_commit(bar(B_EMPTY + slot));
+                    if (j + 1 == cur.nkv - 1) tc_commit(bar(B_QEMPTY));
                 }
                 __syncwarp();
+            } else {
+                if (!(ok = read_item(n, nxt))) break;
+                ++n;
+                has_next = nxt.nkv > 0;
+                if (has_next && !(ok = first_qk(nxt, item_no + 1))) break;
             }
-            const int i = load_index_v(j, nkv), slot = i % kRing;
-            ok = tc_warp_wait(bar(B_P + h), j & 1, abort_flag) &&
-                 tc_warp_wait(bar(B_FULL + slot), (i / kRing) & 1, abort_flag);
-            if (ok && j == nkv - 1 && zero_tail) ok = tc_warp_wait(bar(B_VZ), 0, abort_flag);
-            if (!ok) break;
+            // PV of tile j of the current item
+            int slot;
+            if (!(ok = tc_warp_wait(bar(B_P + h), static_cast<uint32_t>(t & 1), abort_flag) && next_load(slot)))
+                break;
+            const int last_valid = cur.n_end - (cur.nkv - 1) * BN;
+            if (j == cur.nkv - 1 && last_valid < BN) {
+                // The last tile may hold rows past the keys (unwritten slots or another prompt):
+                // zero them before any PV reads them (P is zero there, but 0 * NaN is not).
+                if (h == 0) {
+                    unsigned char *vt = smem + OFF_RING + slot * kTile;
+                    for (int c = lane; c < (BN - last_valid) * 16; c += 32) {  // 16-byte chunks
+                        const int r = last_valid + c / 16, c16 = c % 16;
+                        *reinterpret_cast<uint4 *>(vt + (c16 >> 3) * kHalf + r * 128 + (c16 & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_VZ));
+                } else if (!(ok = tc_warp_wait(bar(B_VZ), zt & 1, abort_flag))) {
+                    break;
+                }
+                ++zt;
+            }
+            // the previous item's output must be out of TMEM before its O is overwritten
+            if (j == 0 && item_no > 0 && !(ok = tc_warp_wait(bar(B_OFREE + h), (item_no - 1) & 1, abort_flag)))
+                break;
             tc_fence_after();
             if (lane == 0) {
-                pv(slot, j);
+                pv(slot, j > 0);
                 tc_commit(bar(B_O + h));
                 tc_commit(bar(B_EMPTY + slot));
             }
             __syncwarp();
+            ++t;
+            if (++j == cur.nkv) {
+                if (!has_next) break;
+                cur = nxt;
+                j = 0;
+                ++item_no;
+            }
         }
         if (!ok && lane == 0) tc_abort(p.err, abort_flag);
         // every MMA this thread issued has finished before the TMEM can be freed
@@ -328,60 +427,71 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const uint32_t srow = tmem + lane_off + (h ? 128 : 0);
         const uint32_t orow = tmem + lane_off + 256 + (h ? 128 : 0);
         unsigned char *prow = smem + (h ? OFF_PB : OFF_PA) + r * 128;  // this row of P, half 0
-        const int hq = h ? hB : hA;
-        const int lim = p.causal ? min(kl, P + m0 + r + 1) : kl;  // keys this row may see
         const uint32_t s_full = bar(B_S + h), s_free = bar(B_F + h), p_full = bar(B_P + h);
-        const uint32_t o_done = bar(B_O + h);
-        float m_use = -INFINITY, l = 0.f;
+        const uint32_t o_done = bar(B_O + h), o_free = bar(B_OFREE + h);
+        long long t = 0;  // tiles of this head so far
         bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            if (!(ok = tc_warp_wait(s_full, j & 1, abort_flag))) break;
-            tc_fence_after();
-            uint32_t sv[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t(&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c);
-                tmem_ld32(srow + c * 32, chunk);
-            }
-            tmem_wait_ld();
-            // S may be overwritten by the next tile's QK from here on
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);
-            const int n0 = j * BN;
-            if (n0 + BN > lim) {
-#pragma unroll
-                for (int e = 0; e < 128; ++e)
-                    if (n0 + e >= lim) sv[e] = 0xff800000u;  // -inf
-            }
-            // row maximum of the raw scores (the scale is positive, so it is applied once)
-            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int e = 0; e < 128; ++e) mq[e & 3] = fmaxf(mq[e & 3], __uint_as_float(sv[e]));
-            const float mraw = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-            const float mx = mraw == -INFINITY ? -INFINITY : mraw * p.scale_log2;
-            // move the reference max only when it grew by more than 2^8 (or was unset)
-            const bool need = mx > m_use + 8.f;
-            const float f = need ? fast_exp2(m_use - mx) : 1.f;  // 0 while m_use is unset
-            if (need) m_use = mx;
-            const float mu = m_use == -INFINITY ? 0.f : m_use;
-            // p = 2^(s * scale - m) on fp32 pairs, packed to 16-bit pairs
-            const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-mu, -mu);
-            uint64_t l2 = f2_pack(0.f, 0.f);
-            uint32_t pk[64];
-#pragma unroll
-            for (int e = 0; e < 128; e += 2) {
-                const uint64_t x2 = f2_fma(u2_pack(sv[e], sv[e + 1]), sc2, nm2);
-                const float p0 = fast_exp2(f2_lo(x2)), p1 = fast_exp2(f2_hi(x2));
-                l2 = f2_add(l2, f2_pack(p0, p1));
-                pk[e >> 1] = E::pack2(p0, p1);
-            }
-            l = l * f + (f2_lo(l2) + f2_hi(l2));
-            // P(j-1) has been consumed and O(j-1) is complete
-            if (j > 0) {
-                if (!(ok = tc_warp_wait(o_done, (j - 1) & 1, abort_flag))) break;
+        ItemInfo it{};
+        for (int n = 0; ok; ++n) {
+            if (!(ok = read_item(n, it)) || it.nkv == 0) break;
+            const int lim = p.causal ? min(it.kl, it.P + it.m0 + r + 1) : it.kl;  // keys this row may see
+            float m_use = -INFINITY, l = 0.f;
+            for (int j = 0; j < it.nkv; ++j, ++t) {
+                if (!(ok = tc_warp_wait(s_full, static_cast<uint32_t>(t & 1), abort_flag))) break;
                 tc_fence_after();
-                if (__any_sync(kFull, need)) {
+                uint32_t sv[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t(&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * c);
+                    tmem_ld32(srow + c * 32, chunk);
+                }
+                tmem_wait_ld();
+                // S may be overwritten by the next tile's QK from here on
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free);
+                const int n0 = j * BN;
+                if (n0 + BN > lim) {
+#pragma unroll
+                    for (int e = 0; e < 128; ++e)
+                        if (n0 + e >= lim) sv[e] = 0xff800000u;  // -inf
+                }
+                // row maximum of the raw scores (the scale is positive, so it is applied once)
+                float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int e = 0; e < 128; ++e) mq[e & 3] = fmaxf(mq[e & 3], __uint_as_float(sv[e]));
+                const float mraw = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+                const float mx = mraw == -INFINITY ? -INFINITY : mraw * p.scale_log2;
+                // move the reference max only when it grew by more than 2^8 (or was unset)
+                const bool need = mx > m_use + 8.f;
+                const float f = need ? fast_exp2(m_use - mx) : 1.f;  // 0 while m_use is unset
+                if (need) m_use = mx;
+                const float mu = m_use == -INFINITY ? 0.f : m_use;
+                // p = 2^(s * scale - m) on fp32 pairs, packed to 16-bit pairs
+                const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-mu, -mu);
+                uint64_t l2 = f2_pack(0.f, 0.f);
+                uint32_t pk[64];
+#pragma unroll
+                for (int e = 0; e < 128; e += 2) {
+                    const uint64_t x2 = f2_fma(u2_pack(sv[e], sv[e + 1]), sc2, nm2);
+                    const float p0 = fast_exp2(f2_lo(x2)), p1 = fast_exp2(f2_hi(x2));
+                    l2 = f2_add(l2, f2_pack(p0, p1));
+                    pk[e >> 1] = E::pack2(p0, p1);
+                }
+                l = l * f + (f2_lo(l2) + f2_hi(l2));
+                // the previous tile's PV has consumed P and completed O
+                if (t > 0) {
+                    if (!(ok = tc_warp_wait(o_done, static_cast<uint32_t>((t - 1) & 1), abort_flag))) break;
+                    tc_fence_after();
+                }
+                // P row r: 16-byte chunk q of half q / 8 sits at chunk (q % 8) ^ (r % 8) of the
+                // 128-byte row (the 128-byte swizzle the MMA descriptor names)
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    *reinterpret_cast<uint4 *>(prow + (q >> 3) * kHalf + (((q & 7) ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                // O(t - 1) is complete: rescale it before this tile's PV adds to it
+                if (j > 0 && __any_sync(kFull, need)) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t ov[32];
@@ -393,42 +503,50 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     }
                     tmem_wait_st();
                 }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
             }
-            // P row r: 16-byte chunk q of half q / 8 sits at chunk (q % 8) ^ (r % 8) of the
-            // 128-byte row (the 128-byte swizzle the MMA descriptor names)
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-                *reinterpret_cast<uint4 *>(prow + (q >> 3) * kHalf + (((q & 7) ^ (r & 7)) << 4)) =
-                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
-        }
-        if (ok) ok = tc_warp_wait(o_done, (nkv - 1) & 1, abort_flag);
-        if (!ok) {
-            if (lane == 0) tc_abort(p.err, abort_flag);
-        } else {
+            if (ok) ok = tc_warp_wait(o_done, static_cast<uint32_t>((t - 1) & 1), abort_flag);
+            if (!ok) break;
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            T *orow_g = out + (static_cast<size_t>(q0 + m0 + r) * p.Hq + hq) * HD;
+            uint32_t ov[64];  // the output row, packed
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
                 tmem_ld32(orow + c * 32, v);
                 tmem_wait_ld();
-                uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2)
-                    pk[e >> 1] = E::pack2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
-                if (r < mrows) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow_g + c * 32);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                }
+                    ov[c * 16 + (e >> 1)] = E::pack2(__uint_as_float(v[e]) * inv, __uint_as_float(v[e + 1]) * inv);
             }
+            // O is out of TMEM: the next item's first PV may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free);
+            // The warp's 32 rows go out through their own rows of the P buffer (swizzled like P),
+            // so that each global store instruction writes two whole 256-byte rows instead of
+            // 16 bytes of 32 rows 4 KB apart.
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                *reinterpret_cast<uint4 *>(prow + (c >> 3) * kHalf + (((c & 7) ^ (r & 7)) << 4)) =
+                    make_uint4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
+            __syncwarp();
+            const unsigned char *pw = smem + (h ? OFF_PB : OFF_PA);
+#pragma unroll 4
+            for (int i = 0; i < 16; ++i) {
+                const int k = i * 32 + lane, rr = quarter * 32 + (k >> 4), c = k & 15;
+                const uint4 u = *reinterpret_cast<const uint4 *>(pw + (c >> 3) * kHalf + rr * 128 +
+                                                                 (((c & 7) ^ (rr & 7)) << 4));
+                if (rr < it.mrows)
+                    *reinterpret_cast<uint4 *>(out + (static_cast<size_t>(it.q0 + it.m0 + rr) * p.Hq +
+                                                      2 * it.pair + h) * HD + c * 8) = u;
+            }
+            __syncwarp();  // the rows are read before the next tile's P overwrites them
         }
+        if (!ok && lane == 0) tc_abort(p.err, abort_flag);
     }
     // ------------------------------------------------------------------------------------------
     tc_fence_before();
@@ -436,6 +554,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     if (warp == 1) {
         tc_fence_after();
         tmem_free(tmem, 512);
+    }
+    // the last CTA to finish resets the work counter for the next launch
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1ull) == gridDim.x - 1) {
+            p.sched[0] = 0;
+            p.sched[1] = 0;
+            __threadfence();
+        }
     }
 }
 
@@ -466,6 +593,25 @@ bool encode_rows(CUtensorMap *m, const void *base, pa_dtype dt, int heads, long 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Work counters of the persistent launches: [slot][0] the next work item, [slot][1] CTAs done.
+// Each launch takes the next slot, so launches in flight on different streams do not share one,
+// and its last CTA resets the pair to zero for the launch that takes the slot next.
+constexpr int kSchedSlots = 64;
+__device__ unsigned long long g_sched[kSchedSlots][2];
+
+unsigned long long *sched_slot() {
+    static std::atomic<unsigned> next{0};
+    static unsigned long long *base[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!base[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_sched) != cudaSuccess) return nullptr;
+        base[dev] = static_cast<unsigned long long *>(ptr);
+    }
+    return base[dev] + 2 * (next.fetch_add(1u) % kSchedSlots);
+}
+
 template <class E>
 cudaError_t launch_tc_typed(const TcParams &prm, cudaStream_t stream) {
     auto kern = prefill_tc_kernel<E>;
@@ -478,8 +624,8 @@ cudaError_t launch_tc_typed(const TcParams &prm, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev] = 1;
     }
-    dim3 grid((prm.max_seqlen_q + BM - 1) / BM, prm.Hq / 2, prm.S);
-    kern<<<grid, kThreads, kSmem, stream>>>(prm);
+    const long long ctas = prm.n_items < device_sm_count() ? prm.n_items : device_sm_count();
+    kern<<<static_cast<unsigned>(ctas > 0 ? ctas : 1), kThreads, kSmem, stream>>>(prm);
     return cudaGetLastError();
 }
 
@@ -495,8 +641,10 @@ int tc_box_rows(const PrefillArgs &a) {
 }
 
 bool tc_prefill_supported(const PrefillArgs &a) {
+    // the output rows leave as 16-byte stores
+    const bool out_aligned = (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
     return a.D == 128 && (a.Hq / a.Hkv) % 2 == 0 && tc_box_rows(a) >= 8 && a.total_q > 0 &&
-           (a.block_tables ? true : a.total_k > 0);
+           (a.block_tables ? true : a.total_k > 0) && out_aligned;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
@@ -524,6 +672,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     prm.causal = a.causal;
     prm.max_seqlen_q = a.max_seqlen_q;
     prm.box_rows = R;
+    prm.row_blocks = (a.max_seqlen_q + BM - 1) / BM;
+    prm.pairs = a.Hq / 2;
+    prm.n_items = static_cast<long long>(prm.row_blocks) * prm.pairs * a.S;
+    prm.sched = sched_slot();
+    if (!prm.sched) return cudaErrorInvalidDevice;
     prm.geom.block_size = a.block_size;
     prm.geom.shift = log2_if_pow2(a.block_size);
     prm.scale_log2 = a.scale * kLog2e;
