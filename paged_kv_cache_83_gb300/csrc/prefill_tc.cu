@@ -81,7 +81,7 @@ static_assert(kSmem <= 232448, "shared memory per CTA");
 constexpr unsigned kFull = 0xffffffffu;
 
 struct TcParams {
-    CUtensorMap tm_q, tm_k, tm_v;  // q: [total_q, Hq, 128]; k, v: [rows, Hkv, 128]; boxes [.,1,64]
+    CUtensorMap tm_q, tm_k, tm_v, tm_o;  // q, out: [total_q, Hq, 128]; k, v: [rows, Hkv, 128]; boxes [.,1,64]
     const int32_t *cu_q, *cu_k, *block_tables;
     void *out;
     int32_t *err;
@@ -485,7 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     tc_fence_after();
                 }
                 // P row r: 16-byte chunk q of half q / 8 sits at chunk (q % 8) ^ (r % 8) of the
-                // 128-byte row (the 128-byte swizzle the MMA descriptor names)
+                // 128-byte row (the 128-byte swizzle the MMA descriptor names). The warp's rows
+                // may still be the source of the previous item's output store.
+                if (j == 0) {
+                    if (lane == 0) bulk_wait_read();
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int q = 0; q < 16; ++q)
                     *reinterpret_cast<uint4 *>(prow + (q >> 3) * kHalf + (((q & 7) ^ (r & 7)) << 4)) =
@@ -526,26 +531,39 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free);
-            // The warp's 32 rows go out through their own rows of the P buffer (swizzled like P),
-            // so that each global store instruction writes two whole 256-byte rows instead of
-            // 16 bytes of 32 rows 4 KB apart.
+            // The warp's 32 rows go out through their own rows of the P buffer (swizzled like P):
+            // two TMA stores when all 32 rows belong to the item, else row-wide 16-byte stores.
 #pragma unroll
             for (int c = 0; c < 16; ++c)
                 *reinterpret_cast<uint4 *>(prow + (c >> 3) * kHalf + (((c & 7) ^ (r & 7)) << 4)) =
                     make_uint4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
-            __syncwarp();
             const unsigned char *pw = smem + (h ? OFF_PB : OFF_PA);
+            if (quarter * 32 + 32 <= it.mrows) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int row0 = it.q0 + it.m0 + quarter * 32;
+                    for (int half = 0; half < 2; ++half)
+                        tma_store_3d(&p.tm_o, half * 64, 2 * it.pair + h, row0,
+                                     smem_addr(pw + half * kHalf + quarter * 32 * 128));
+                    bulk_commit();
+                }
+            } else {
+                __syncwarp();
 #pragma unroll 4
-            for (int i = 0; i < 16; ++i) {
-                const int k = i * 32 + lane, rr = quarter * 32 + (k >> 4), c = k & 15;
-                const uint4 u = *reinterpret_cast<const uint4 *>(pw + (c >> 3) * kHalf + rr * 128 +
-                                                                 (((c & 7) ^ (rr & 7)) << 4));
-                if (rr < it.mrows)
-                    *reinterpret_cast<uint4 *>(out + (static_cast<size_t>(it.q0 + it.m0 + rr) * p.Hq +
-                                                      2 * it.pair + h) * HD + c * 8) = u;
+                for (int i = 0; i < 16; ++i) {
+                    const int k = i * 32 + lane, rr = quarter * 32 + (k >> 4), c = k & 15;
+                    const uint4 u = *reinterpret_cast<const uint4 *>(pw + (c >> 3) * kHalf + rr * 128 +
+                                                                     (((c & 7) ^ (rr & 7)) << 4));
+                    if (rr < it.mrows)
+                        *reinterpret_cast<uint4 *>(out + (static_cast<size_t>(it.q0 + it.m0 + rr) * p.Hq +
+                                                          2 * it.pair + h) * HD + c * 8) = u;
+                }
             }
             __syncwarp();  // the rows are read before the next tile's P overwrites them
         }
+        if (lane == 0) bulk_wait_all();  // the output stores are complete before the CTA exits
+        __syncwarp();
         if (!ok && lane == 0) tc_abort(p.err, abort_flag);
     }
     // ------------------------------------------------------------------------------------------
@@ -641,7 +659,7 @@ int tc_box_rows(const PrefillArgs &a) {
 }
 
 bool tc_prefill_supported(const PrefillArgs &a) {
-    // the output rows leave as 16-byte stores
+    // the output rows leave through TMA stores and 16-byte stores
     const bool out_aligned = (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
     return a.D == 128 && (a.Hq / a.Hkv) % 2 == 0 && tc_box_rows(a) >= 8 && a.total_q > 0 &&
            (a.block_tables ? true : a.total_k > 0) && out_aligned;
@@ -656,7 +674,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
                                            : static_cast<long long>(a.total_k);
     if (!encode_rows(&prm.tm_q, a.q, a.dtype, a.Hq, a.total_q, 128) ||
         !encode_rows(&prm.tm_k, kb, a.dtype, a.Hkv, krows, R) ||
-        !encode_rows(&prm.tm_v, vb, a.dtype, a.Hkv, krows, R))
+        !encode_rows(&prm.tm_v, vb, a.dtype, a.Hkv, krows, R) ||
+        !encode_rows(&prm.tm_o, a.out, a.dtype, a.Hq, a.total_q, 32))
         return cudaErrorInvalidValue;
     prm.cu_q = a.cu_q;
     prm.cu_k = a.cu_k;
