@@ -1,7 +1,7 @@
 """Benchmark of the paged KV-cache hot path on GB300.
 
-One step is one decode layer-step of the whole hot path: pa_store_kv (the step's new K/V rows
-into the pool) then pa_decode (split-K paged GQA decode + merge), over the
+One step is one decode layer-step of the whole hot path: pa_store_decode (the step's new K/V
+rows into the pool and the split-K paged GQA decode in one launch, + the merge), over the
 ``qwen3_06b_decode`` workload (256 sequences, contexts U[100, 4096], 16/8 heads, D 128,
 256-token blocks, bf16). Two layers' pools are used in turn so that consecutive steps read
 different data; each pool (2.7 GB) is far larger than the 129 MB L2.
@@ -10,14 +10,15 @@ Headline: KV bytes the step must read (every cached row of K and V once per kv h
 by the device time of the step, in GB/s, and as a fraction of the measured HBM peak; decode
 steps per second per layer. The same line carries:
 
-* ``roofline``: the pa_decode call (split kernel + merge) timed alone with CUDA events inside
+* ``roofline``: the step's call (split kernel + merge) timed alone with CUDA events inside
   the timed region, against the measured copy bandwidth;
 * ``e2e``: the same metric when every step also copies its inputs from pinned host memory and
   reads the output back, synchronising each step (the pool stays resident, as in an engine);
 * ``cpu_baseline``: the fp64 CPU oracle on a bounded sample of the same workload, on the
   host's cores;
-* ``rows``: the other rows of the path measured the same way: the store alone, and the
-  varlen prefill with a 512-token cached prefix (``prefill_prefix``) with its store.
+* ``rows``: the other rows of the path measured the same way: the same step as two calls
+  (pa_store_kv, then pa_decode), the store alone, the varlen prefill with a 512-token cached
+  prefix (``prefill_prefix``) with its store, and the two small decode workloads as CUDA graphs.
 
 ``--impl reference`` times the CPU oracle as the reference arm, on the same metric.
 Multi-GPU (torchrun): every rank runs an independent replica (the path shards by sequence
@@ -53,8 +54,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # profiles/decode_kernel_qwen3_06b_decode.md and profiles/prefill_tc_kernel_prefill_prefix.md
 # (layer 0 of the default workload; prefill_prefix). Each is valid only for the kernel sources it
 # was taken on, identified by their hash; after any change the bench reports null.
-DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_279_818_544,
-                  "sha256": "7c3c73c81f58a6004f56fe6371f3895d327c3aa6815d22380a8a4201abbc2736"}
+DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_281_701_888,
+                  "sha256": "4d0d0fd0766a3cc4dbe61ee7d8d57f4f09a7a511e0a740b165867b6afa7ca5e8"}
 PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 411_089_920,
                    "sha256": "d56841fd65495c1c9a79fd3c92669449ba16f74585a2c9c6b73af500664f8661"}
 
@@ -270,21 +271,19 @@ def run_gpu(args, ws_, rank, local):
     nl = len(layers)
     plan_splits = pa.pa_decode_workspace_size(c0.B, c0.Hq, c0.Hkv, c0.D, c0.max_blocks_per_seq,
                                               c0.block_size) > 0
-    launches_per_step = 2 + (1 if plan_splits else 0)
+    # one layer step = pa_store_decode: the store of the new token and the decode in one launch
+    # (+ the merge kernel when contexts are split across CTAs)
+    launches_per_step = 1 + (1 if plan_splits else 0)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
     dec_ev = [(ev(), ev()) for _ in range(args.steps)]
-    st_ev = [(ev(), ev()) for _ in range(args.steps)]
 
     def step(i, timed=False):
         L = layers[i % nl]
         if timed:
-            st_ev[i][0].record(stream)
-        pa.pa_store_kv(L.k_new, L.v_new, L.kc, L.vc, L.sm)
-        if timed:
-            st_ev[i][1].record(stream)
             dec_ev[i][0].record(stream)
-        pa.pa_decode(L.out, L.q, L.kc, L.vc, L.bt, L.cl, L.c.scale, workspace=L.ws)
+        pa.pa_store_decode(L.out, L.q, L.k_new, L.v_new, L.kc, L.vc, L.bt, L.cl, L.c.scale,
+                           workspace=L.ws)
         if timed:
             dec_ev[i][1].record(stream)
 
@@ -318,7 +317,19 @@ def run_gpu(args, ws_, rank, local):
 
     elapsed = t0.elapsed_time(t1)  # ms
     dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
-    st_ms = [a.elapsed_time(b) for a, b in st_ev]
+    # the same step as two calls (pa_store_kv, then pa_decode), for comparison
+    n2 = max(3, min(args.steps, 200))
+    st_ev = [(ev(), ev(), ev()) for _ in range(n2)]
+    for i in range(n2):
+        L = layers[i % nl]
+        st_ev[i][0].record(stream)
+        pa.pa_store_kv(L.k_new, L.v_new, L.kc, L.vc, L.sm)
+        st_ev[i][1].record(stream)
+        pa.pa_decode(L.out, L.q, L.kc, L.vc, L.bt, L.cl, L.c.scale, workspace=L.ws)
+        st_ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    st_ms = [a.elapsed_time(b) for a, b, _ in st_ev]
+    two_ms = [a.elapsed_time(c) for a, _, c in st_ev]
     if dist is not None:
         tt = torch.tensor([elapsed], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -335,8 +346,8 @@ def run_gpu(args, ws_, rank, local):
     # ---- e2e: inputs from pinned host memory each step, output read back each step ----
     L = layers[0]
     pin = lambda t: t.cpu().pin_memory()
-    h_in = [pin(x) for x in (L.q, L.k_new, L.v_new, L.sm, L.bt, L.cl)]
-    d_in = [torch.empty_like(x) for x in (L.q, L.k_new, L.v_new, L.sm, L.bt, L.cl)]
+    h_in = [pin(x) for x in (L.q, L.k_new, L.v_new, L.bt, L.cl)]
+    d_in = [torch.empty_like(x) for x in (L.q, L.k_new, L.v_new, L.bt, L.cl)]
     h_out = torch.empty(L.out.shape, dtype=L.out.dtype).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in h_in)
     d2h = h_out.numel() * h_out.element_size()
@@ -345,9 +356,8 @@ def run_gpu(args, ws_, rank, local):
     def e2e_step():
         for h, d in zip(h_in, d_in):
             d.copy_(h, non_blocking=True)
-        q, kn, vn, sm, bt, cl = d_in
-        pa.pa_store_kv(kn, vn, L.kc, L.vc, sm)
-        pa.pa_decode(L.out, q, L.kc, L.vc, bt, cl, L.c.scale, workspace=L.ws)
+        q, kn, vn, bt, cl = d_in
+        pa.pa_store_decode(L.out, q, kn, vn, L.kc, L.vc, bt, cl, L.c.scale, workspace=L.ws)
         h_out.copy_(L.out, non_blocking=True)
         stream.synchronize()
 
@@ -379,8 +389,13 @@ def run_gpu(args, ws_, rank, local):
     rows["store_kv_decode"] = {"kernel": "store_kv_kernel", "ms": st_mean,
                                "GB_per_s": st_bytes / (st_mean * 1e-3) / 1e9,
                                "bytes": st_bytes, "note": "256 new rows: launch-latency bound"}
-    rows["decode"] = {"kernel": "decode_kernel + decode_merge_kernel", "ms": dec_mean,
+    rows["decode"] = {"kernel": "pa_store_decode: decode_kernel (+ the new token's store) + "
+                                "decode_merge_kernel", "ms": dec_mean,
                       "GB_per_s": achieved, "frac_of_hbm": achieved / hbm}
+    rows["two_call_step"] = {"calls": "pa_store_kv + pa_decode", "ms": statistics.mean(two_ms),
+                             "GB_per_s": kv_bytes(c0.context_lens, c0.Hkv, c0.D) /
+                             (statistics.mean(two_ms) * 1e-3) / 1e9,
+                             "note": "layer 0's KV bytes; the fused call is the step"}
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -408,13 +423,13 @@ def run_gpu(args, ws_, rank, local):
         "decode_steps_per_sec_per_layer": 1e3 / ms_step,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
-                     "kernel": "pa_decode: decode_kernel + decode_merge_kernel",
+                     "kernel": "pa_store_decode: decode_kernel + decode_merge_kernel",
                      "peak_source": f"{pk_kind} hbm_gbs"},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e_steps,
-                "note": "pool resident; per step: H2D of q, new K/V, slots, tables, lengths; "
-                        "store + decode; D2H of the output; stream sync"},
+                "note": "pool resident; per step: H2D of q, new K/V, tables, lengths; "
+                        "pa_store_decode; D2H of the output; stream sync"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "rows": rows,
@@ -440,19 +455,23 @@ def bench_small_decode(torch, pa, dev, hbm) -> dict:
                   for l in range(n_layers)]
         kv = statistics.mean(kv_bytes(L.c.context_lens, L.c.Hkv, L.c.D) for L in layers)
 
-        def body(with_store):
+        def body(mode):
             for L in layers:
-                if with_store:
+                if mode == "fused":
+                    pa.pa_store_decode(L.out, L.q, L.k_new, L.v_new, L.kc, L.vc, L.bt, L.cl,
+                                       L.c.scale, workspace=L.ws)
+                    continue
+                if mode == "two":
                     pa.pa_store_kv(L.k_new, L.v_new, L.kc, L.vc, L.sm)
                 pa.pa_decode(L.out, L.q, L.kc, L.vc, L.bt, L.cl, L.c.scale, workspace=L.ws)
 
         us = {}
-        for with_store in (True, False):
-            body(with_store)
+        for mode in ("fused", "two", "decode"):
+            body(mode)
             torch.cuda.synchronize()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                body(with_store)
+                body(mode)
             for _ in range(3):
                 g.replay()
             torch.cuda.synchronize()
@@ -464,14 +483,15 @@ def bench_small_decode(torch, pa, dev, hbm) -> dict:
                 b.record()
                 torch.cuda.synchronize()
                 ts.append(a.elapsed_time(b))
-            us[with_store] = statistics.median(ts) * 1e3 / n_layers
+            us[mode] = statistics.median(ts) * 1e3 / n_layers
             del g
         c = layers[0].c
         res[name] = {"seqs": c.B, "Hq": c.Hq, "Hkv": c.Hkv, "D": c.D, "block_size": c.block_size,
                      "dtype": c.dtype, "kv_bytes_per_layer": int(kv), "layers_in_graph": n_layers,
-                     "us_store_plus_decode_per_layer": us[True], "us_decode_per_layer": us[False],
-                     "decode_GB_per_s": kv / (us[False] * 1e-6) / 1e9,
-                     "frac_of_hbm": kv / (us[False] * 1e-6) / 1e9 / hbm,
+                     "us_store_decode_per_layer": us["fused"],
+                     "us_store_then_decode_per_layer": us["two"], "us_decode_per_layer": us["decode"],
+                     "decode_GB_per_s": kv / (us["decode"] * 1e-6) / 1e9,
+                     "frac_of_hbm": kv / (us["decode"] * 1e-6) / 1e9 / hbm,
                      "l2": f"{n_layers} layers x {pool_bytes / 1e6:.1f} MB of pools per graph replay"}
         del layers
         torch.cuda.empty_cache()

@@ -132,6 +132,30 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
                     size_t workspace_bytes, int32_t *err, cudaStream_t stream);
 
 /*
+ * pa_store_decode: the decode layer step (store the new token's K/V, then decode) in one launch.
+ *
+ * Source: "nano-vLLM Part 4" section 3 (each decode step writes the new token's key and value into
+ * the cache through the slot mapping, then attends over the cached history); "mini-vLLM" (one
+ * token per sequence attending to that sequence's cached keys and values).
+ *
+ * For sequence i with n = context_lens[i] > 0 the new token is position n - 1: its rows k_new[i],
+ * v_new[i] are written to the slot of that position, block_tables[i][(n-1) / block_size] *
+ * block_size + (n-1) % block_size, and the attention uses them for that position directly (the
+ * launch does not read them back from the pool). The result, pools included, equals pa_store_kv
+ * with slot_mapping[i] = that slot (or -1 when n == 0) followed by pa_decode.
+ *
+ * k_new, v_new  [B, Hkv, D], 16-byte aligned. Rows of sequences with n == 0 are not stored.
+ * Other arguments, the workspace and the errors as pa_decode. The new token's slot must not be
+ * read by another sequence of the same call (a block with free slots belongs to one sequence).
+ */
+pa_status pa_store_decode(void *out, const void *q, const void *k_new, const void *v_new,
+                          void *k_cache, void *v_cache, const int32_t *block_tables,
+                          int max_blocks_per_seq, const int32_t *context_lens, int B, int Hq,
+                          int Hkv, int D, int block_size, int num_blocks, float scale,
+                          pa_dtype dtype, void *workspace, size_t workspace_bytes, int32_t *err,
+                          cudaStream_t stream);
+
+/*
  * pa_prefill_varlen: variable-length (causal) prefill attention over packed prompts, with a
  * cached prefix read from the pool.
  *

@@ -4,8 +4,9 @@ prefill with a cached prefix, as hand-written sm_103a CUDA kernels behind a C AB
 library in-tree."""
 from .binding import (PA_DECODE_NOALLOC_SCRATCH_BYTES, PA_DEVERR_LENGTH, PA_DEVERR_SLOT,
                       PA_DEVERR_TABLE, PagedAttnError, load, pa_decode, pa_decode_noalloc,
-                      pa_decode_workspace_size, pa_prefill_varlen, pa_store_kv)
+                      pa_decode_workspace_size, pa_prefill_varlen, pa_store_decode, pa_store_kv)
 
-__all__ = ["load", "pa_store_kv", "pa_decode", "pa_decode_workspace_size", "pa_prefill_varlen",
+__all__ = ["load", "pa_store_kv", "pa_decode", "pa_store_decode", "pa_decode_workspace_size",
+           "pa_prefill_varlen",
            "pa_decode_noalloc", "PA_DECODE_NOALLOC_SCRATCH_BYTES",
            "PagedAttnError", "PA_DEVERR_SLOT", "PA_DEVERR_TABLE", "PA_DEVERR_LENGTH"]

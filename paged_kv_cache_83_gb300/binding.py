@@ -17,8 +17,8 @@ LIB_PATH = PKG / "_build" / "libpagedattn.so"
 
 PA_F16, PA_BF16 = 0, 1
 PA_DEVERR_SLOT, PA_DEVERR_TABLE, PA_DEVERR_LENGTH = 1, 2, 4
-EXPORTS = ("pa_store_kv", "pa_decode_workspace_size", "pa_decode", "pa_prefill_varlen",
-           "pa_decode_noalloc", "pa_status_string")
+EXPORTS = ("pa_store_kv", "pa_decode_workspace_size", "pa_decode", "pa_store_decode",
+           "pa_prefill_varlen", "pa_decode_noalloc", "pa_status_string")
 PA_DECODE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 _lib = None
@@ -46,6 +46,8 @@ def load(path: Path | str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_decode_workspace_size.restype = Z
     lib.pa_decode.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, P, Z, P, P]
     lib.pa_decode.restype = I
+    lib.pa_store_decode.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, P, Z, P, P]
+    lib.pa_store_decode.restype = I
     lib.pa_prefill_varlen.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, I, I, I, I, I, I,
                                       F, I, I, P, P]
     lib.pa_prefill_varlen.restype = I
@@ -134,6 +136,28 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _i32(block_tables, "block_tables"), maxb,
         _i32(context_lens, "context_lens"), B, Hq, Hkv, D, bs, NB, float(scale), dt,
         _ptr(workspace), ws_bytes, _i32(err, "err"), _stream(stream)))
+
+
+def pa_store_decode(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                    scale: float, workspace=None, err=None, stream=None) -> None:
+    """Store the new tokens' rows k_new, v_new [B, Hkv, D] at position context_lens - 1 of each
+    sequence and decode, in one launch (= pa_store_kv, then pa_decode)."""
+    NB, bs, Hkv, D = k_cache.shape
+    B, Hq, Dq = q.shape
+    if (Dq != D or tuple(out.shape) != (B, Hq, D) or tuple(k_new.shape) != (B, Hkv, D) or
+            tuple(v_new.shape) != (B, Hkv, D) or block_tables.shape[0] != B or
+            context_lens.shape != (B,)):
+        raise ValueError("shape mismatch")
+    dt = _dtype(q)
+    if any(t.dtype != q.dtype for t in (out, k_new, v_new, k_cache, v_cache)):
+        raise TypeError("q, out, the new rows and the pools must share a dtype")
+    maxb = block_tables.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("pa_store_decode", load().pa_store_decode(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _i32(block_tables, "block_tables"), maxb, _i32(context_lens, "context_lens"), B, Hq, Hkv,
+        D, bs, NB, float(scale), dt, _ptr(workspace), ws_bytes, _i32(err, "err"),
+        _stream(stream)))
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,

@@ -58,6 +58,7 @@ constexpr int kSlot1 = 8;  // partial segment that is not the CTA's first: works
 struct TileMeta {
     int b, g, flags, all_valid;  // all_valid: every one of the 128 rows is a context position
     unsigned long long valid[2];  // bit r of the 128-bit mask: tile row r is a context position
+    int newrow, pad;              // row whose K/V are in the spare row (a new token), or -1
 };
 
 // What the merge kernel needs to know about one CTA.
@@ -71,6 +72,8 @@ struct SegRecord {
 struct DecodeParams {
     CUtensorMap tmap_k, tmap_v;  // [slots, Hkv, D] views of the pools, box [box_rows, 1, D]
     const void *q;
+    const void *k_new, *v_new;  // fused store: the new tokens' rows [B, Hkv, D], or null
+    void *k_cache, *v_cache;    // the pools (written by the fused store only)
     const int32_t *block_tables, *context_lens;
     void *out;
     float *part;     // [P][2][G][D + 2]: normalised O, max (log2 units), sum
@@ -100,7 +103,8 @@ struct Shape {
     static constexpr int PV_IT = kWPos / RPI;
     static constexpr int HPR = 32 / kWPos;                    // softmax heads per round
     static constexpr int ROUNDS = (G + HPR - 1) / HPR;
-    static constexpr int TILE_BYTES = kTN * D * 2;
+    // 64 rows + a spare row that takes a new token's K (or V) row in the fused store + decode
+    static constexpr int TILE_BYTES = (kTN + 1) * D * 2;
     static constexpr int Q_BYTES = G * D * 2;
     static constexpr int STAGE_BYTES = (2 * TILE_BYTES + Q_BYTES + 1023) / 1024 * 1024;
     static constexpr int RED_BYTES = kConsumers * G * (D + 2) * 4;
@@ -354,6 +358,10 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
             if (last && seg_t0 == 0 && pt == pnt - 1) flags |= kWhole;
             if (!first_seg) flags |= kSlot1;
             if (first) bytes += S::Q_BYTES;
+            // fused store: the pair's last tile holds the new token (position pn - 1); its rows
+            // come from k_new / v_new into the spare rows, not from the pool
+            const bool new_tok = p.k_new != nullptr && pt == pnt - 1;
+            if (new_tok) bytes += 2 * D * 2;
 
             unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
             if (lane == 0) {
@@ -364,6 +372,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
                 m.all_valid = (vw[0] & vw[1] & vw[2] & vw[3]) == 0xffffffffu;
                 m.valid[0] = (static_cast<unsigned long long>(vw[1]) << 32) | vw[0];
                 m.valid[1] = (static_cast<unsigned long long>(vw[3]) << 32) | vw[2];
+                m.newrow = new_tok ? (pn - 1) - pos0 : -1;
+                m.pad = 0;
                 metas[stage] = m;
                 mbar_arrive_expect_tx(full0 + 8 * stage, bytes);
             }
@@ -380,6 +390,29 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
             if (first && lane == 0) {
                 const T *qsrc = static_cast<const T *>(p.q) + (static_cast<size_t>(pb_) * p.Hq + pg * G) * D;
                 bulk_load(kdst + 2 * S::TILE_BYTES, qsrc, S::Q_BYTES, full0 + 8 * stage);
+            }
+            if (new_tok) {
+                const size_t row_off = (static_cast<size_t>(pb_) * p.Hkv + pg) * D;
+                if (lane == 0) {
+                    bulk_load(kdst + kTN * D * 2, static_cast<const T *>(p.k_new) + row_off, D * 2,
+                              full0 + 8 * stage);
+                    bulk_load(vdst + kTN * D * 2, static_cast<const T *>(p.v_new) + row_off, D * 2,
+                              full0 + 8 * stage);
+                }
+                // ... and into the pool, at the slot of position pn - 1 (no copy in this launch
+                // reads that slot's row: the tile takes it from the spare row)
+                const int id = p.block_tables[static_cast<size_t>(pb_) * p.max_blocks + p.geom.block_of(pn - 1)];
+                constexpr int kChunks = D * 2 / 16;  // 16-byte chunks per row
+                if (id >= 0 && id < p.num_blocks && lane < 2 * kChunks) {
+                    const long long slot = static_cast<long long>(id) * p.geom.block_size + p.geom.offset_of(pn - 1);
+                    const bool is_v = lane >= kChunks;
+                    const int c = lane % kChunks;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                                           static_cast<const T *>(is_v ? p.v_new : p.k_new) + row_off) + c;
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(is_v ? p.v_cache : p.k_cache) +
+                                                           (static_cast<size_t>(slot) * p.Hkv + pg) * D) + c;
+                    *dst = *src;
+                }
             }
             ++issued;
             if (last) first_seg = false;
@@ -430,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
             return;
         }
         const TileMeta &m = metas[stage];
-        const int mflags = m.flags, mb = m.b, mg = m.g, mall = m.all_valid;
+        const int mflags = m.flags, mb = m.b, mg = m.g, mall = m.all_valid, mnew = m.newrow;
         const unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
         const uint32_t kb = smem_addr(st), vb = kb + S::TILE_BYTES;
         // this warp's rows as a validity mask (bit rl: row rl of the warp)
@@ -471,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
             uint64_t d2[G][S::CPL];
 #pragma unroll
             for (int c = 0; c < S::CPL; ++c) {
-                const uint4 kv = lds128(kb + row * D * 2 + S::chunk(c, r, u) * 16);
+                const uint4 kv = lds128(kb + (row == mnew ? kTN : row) * D * 2 + S::chunk(c, r, u) * 16);
                 const uint64_t k0 = unpack_pair<E>(kv.x), k1 = unpack_pair<E>(kv.y);
                 const uint64_t k2 = unpack_pair<E>(kv.z), k3 = unpack_pair<E>(kv.w);
 #pragma unroll
@@ -534,7 +567,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
             for (int e = 0; e < S::NPV; ++e) acc[h][e] = f2_mul(acc[h][e], a2);
         }
         auto pv_row = [&](int rl) {
-            const int row = cw * kWPos + rl;
+            const int row0 = cw * kWPos + rl;
+            const int row = row0 == mnew ? kTN : row0;
             uint64_t v[S::NPV];
             if constexpr (S::CPV == 8) {
                 const uint4 vv = lds128(vb + row * D * 2 + cc * 16);
@@ -842,6 +876,10 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
         !encode_pool(&prm.tmap_v, a.v_cache, a.dtype, a.D, a.Hkv, slots, R))
         return cudaErrorInvalidValue;
     prm.q = a.q;
+    prm.k_new = a.k_new;
+    prm.v_new = a.v_new;
+    prm.k_cache = const_cast<void *>(a.k_cache);
+    prm.v_cache = const_cast<void *>(a.v_cache);
     prm.block_tables = a.block_tables;
     prm.context_lens = a.context_lens;
     prm.out = a.out;

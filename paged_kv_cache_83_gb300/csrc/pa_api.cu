@@ -103,6 +103,38 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     return from_cuda(pa::launch_decode(a, plan, stream));
 }
 
+pa_status pa_store_decode(void *out, const void *q, const void *k_new, const void *v_new,
+                          void *k_cache, void *v_cache, const int32_t *block_tables,
+                          int max_blocks_per_seq, const int32_t *context_lens, int B, int Hq,
+                          int Hkv, int D, int block_size, int num_blocks, float scale,
+                          pa_dtype dtype, void *workspace, size_t workspace_bytes, int32_t *err,
+                          cudaStream_t stream) {
+    if (!dtype_ok(dtype)) return PA_ERR_DTYPE;
+    if (B < 0 || max_blocks_per_seq < 0 || block_size < 1 || num_blocks < 0) return PA_ERR_SHAPE;
+    pa_status st = check_heads(Hq, Hkv, D);
+    if (st != PA_OK) return st;
+    if (static_cast<long long>(max_blocks_per_seq) * block_size > INT_MAX) return PA_ERR_SHAPE;
+    if (B > 65535) return PA_ERR_UNSUPPORTED;
+    if (B == 0) return PA_OK;
+    if (!out || !q || !k_new || !v_new || !k_cache || !v_cache || !context_lens ||
+        (max_blocks_per_seq > 0 && !block_tables))
+        return PA_ERR_NULL;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(k_new) || !aligned16(v_new))
+        return PA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(num_blocks) * block_size > INT_MAX) return PA_ERR_UNSUPPORTED;
+    const pa::DecodePlan plan = pa::plan_decode(B, Hq, Hkv, D, max_blocks_per_seq, block_size);
+    if (plan.ws_bytes > 0 && (!workspace || workspace_bytes < plan.ws_bytes || !aligned16(workspace)))
+        return PA_ERR_WORKSPACE;
+    pa::DecodeArgs a{out,  q,         k_cache,           v_cache,    block_tables,
+                     context_lens, B, Hq,                Hkv,        D,
+                     max_blocks_per_seq,  block_size, num_blocks, scale, dtype,
+                     workspace,    err};
+    a.k_new = k_new;
+    a.v_new = v_new;
+    return from_cuda(pa::launch_decode(a, plan, stream));
+}
+
 pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void *v,
                             const void *k_cache, const void *v_cache,
                             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int S,

@@ -37,6 +37,7 @@ struct DecodeArgs {
     pa_dtype dtype;
     void *workspace;
     int32_t *err;
+    const void *k_new = nullptr, *v_new = nullptr;  // fused store + decode: new rows [B, Hkv, D]
 };
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
 

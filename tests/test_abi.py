@@ -29,7 +29,7 @@ def lib():
 
 def test_header_declares_the_three_calls():
     names = declared_functions()
-    for n in ("pa_store_kv", "pa_decode", "pa_prefill_varlen", "pa_decode_workspace_size",
+    for n in ("pa_store_kv", "pa_decode", "pa_store_decode", "pa_prefill_varlen", "pa_decode_workspace_size",
               "pa_status_string"):
         assert n in names
 
@@ -115,3 +115,24 @@ def test_workspace_size_rules(lib):
     small = lib.pa_decode_workspace_size(2, 4, 2, 64, 4, 16)
     big = lib.pa_decode_workspace_size(2, 4, 2, 64, 400, 16)
     assert big >= small
+
+
+def _store_decode(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, kn=FAKE, vn=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, maxb=4, cl=FAKE, B=2,
+             Hq=4, Hkv=2, D=64, bs=16, nb=8, scale=0.125, dt=0, ws=None, wsb=0, err=None, stream=None)
+    a.update(kw)
+    return lib.pa_store_decode(*a.values())
+
+
+def test_store_decode_host_checks(lib):
+    assert _store_decode(lib, dt=2) == 3
+    assert _store_decode(lib, Hq=5) == 2
+    assert _store_decode(lib, D=96) == 4
+    assert _store_decode(lib, bs=0) == 2
+    assert _store_decode(lib, B=0) == 0           # empty batch: no-op
+    assert _store_decode(lib, kn=None) == 1
+    assert _store_decode(lib, vc=None) == 1
+    assert _store_decode(lib, vn=FAKE + 8) == 4   # misaligned new rows
+    need = lib.pa_decode_workspace_size(2, 4, 2, 64, 4, 16)
+    if need:
+        assert _store_decode(lib, ws=None, wsb=0) == 5
