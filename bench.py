@@ -384,6 +384,8 @@ def run_gpu(args, ws_, rank, local):
         rows.update(bench_prefill(torch, pa, dev, stream, bf16_peak, hbm, args))
     if not args.skip_small:
         rows["decode_small_graphs"] = bench_small_decode(torch, pa, dev, hbm)
+    if rank == 0 and not args.skip_cpu:
+        rows["block_manager"] = bench_block_manager(pa)
     st_mean = statistics.mean(st_ms)
     st_bytes = 4 * c0.B * c0.Hkv * c0.D * 2
     rows["store_kv_decode"] = {"kernel": "store_kv_kernel", "ms": st_mean,
@@ -496,6 +498,41 @@ def bench_small_decode(torch, pa, dev, hbm) -> dict:
         del layers
         torch.cuda.empty_cache()
     return res
+
+
+def bench_block_manager(pa) -> dict:
+    """The host block manager on a serving-shaped trace: 256 sequences that share a 512-token
+    system prompt, 256-token blocks; admit all, 256 decode appends each, release all. Timed
+    through the Python binding (one ctypes call per operation, which dominates the per-call
+    times) and, beside it, the reference model in oracle/block_manager.py on the same trace."""
+    from oracle.block_manager import BlockManagerModel
+    rng = np.random.default_rng(7)
+    bs, n_seq, steps = 256, 256, 256
+    system = list(rng.integers(0, 150000, size=512))
+    prompts = [system + list(rng.integers(0, 150000, size=int(rng.integers(100, 1000))))
+               for _ in range(n_seq)]
+    need = sum(-(-(len(t) + steps) // bs) for t in prompts)
+    N = int(need * 1.25)
+    out = {"trace": f"{n_seq} seqs, 512-token shared prefix + U[100,1000), {steps} appends each, "
+                    f"bs {bs}, {N} blocks"}
+    arrays = [np.asarray(p, dtype=np.int32) for p in prompts]  # the library takes int32 arrays
+    for name, make, ps in (("library", lambda: pa.BlockManager(N, bs), arrays),
+                           ("reference_model", lambda: BlockManagerModel(N, bs), prompts)):
+        bm = make()
+        t0 = time.perf_counter()
+        cached = sum(bm.allocate(i, p) for i, p in enumerate(ps))
+        t1 = time.perf_counter()
+        for step in range(steps):
+            for i in range(n_seq):
+                bm.append(i, step)
+        t2 = time.perf_counter()
+        for i in range(n_seq):
+            bm.release(i)
+        t3 = time.perf_counter()
+        out[name] = {"us_per_allocate": (t1 - t0) / n_seq * 1e6,
+                     "us_per_append": (t2 - t1) / (n_seq * steps) * 1e6,
+                     "us_per_release": (t3 - t2) / n_seq * 1e6, "tokens_cached": int(cached)}
+    return out
 
 
 def bench_prefill(torch, pa, dev, stream, bf16_peak, hbm, args) -> dict:

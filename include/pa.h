@@ -225,6 +225,60 @@ pa_status pa_decode_noalloc(void *out, const void *q, const void *k_cache, const
                             int block_size, int num_blocks, float scale, pa_dtype dtype,
                             int32_t *err, cudaStream_t stream);
 
+/*
+ * Host block manager: block ids, reference counts and an exact full-block prefix cache for the
+ * pool, with one block table per sequence. Host code only; nothing here touches the GPU.
+ *
+ * Source: "nano-vLLM Part 4", sections 2 and 3 (the BlockManager's ids, reference counts and
+ * prefix-hash metadata, the exact full-block prefix cache, complete blocks hashed after each step,
+ * blocks freed when a sequence finishes); smzdm nano-vLLM deep dive "调度与内存" (fixed-size blocks,
+ * reference counts, the prefix cache shared by requests with a common system prompt, preemption
+ * that frees blocks and keeps the tokens); "mini-vLLM" (a preallocated pool, an O(1) free-list
+ * allocator, a block table per sequence). The pages give no API; this one is:
+ *
+ *   pa_bm_create        a pool of num_blocks blocks of block_size slots; all free, queued in id
+ *                       order. flags: 0, or PA_BM_DEGENERATE_HASH (every token hash equal, for
+ *                       tests of the collision path). NULL on bad arguments or no memory.
+ *   pa_bm_allocate      blocks for a new sequence `seq` with tokens[0..n): the longest run of
+ *                       cached full blocks that starts it is reused, except a block holding its
+ *                       last token (at least one token is always computed); the other blocks come
+ *                       from the front of the free queue (a free block taken for new content is
+ *                       no longer findable, nor is any block cached after it); the sequence's full
+ *                       blocks are cached at once. Returns the number of tokens already cached (a
+ *                       multiple of block_size, < n), or PA_BM_ERR_NO_BLOCKS with nothing changed.
+ *   pa_bm_can_allocate  1 if pa_bm_allocate would succeed now, else 0.
+ *   pa_bm_append        one more token for `seq`: a new block from the free queue when its last
+ *                       block is full (PA_BM_ERR_NO_BLOCKS with nothing changed if none is free);
+ *                       a block that becomes full is cached. Returns the token's slot
+ *                       (block * block_size + offset), the value pa_store_kv's slot_mapping takes.
+ *   pa_bm_release       the sequence finishes (or is preempted): one reference less on each of
+ *                       its blocks, last block first; blocks left with none join the back of the
+ *                       free queue and stay findable by the cache until taken for new content.
+ *   pa_bm_block_table   writes min(cap, blocks) entries of the sequence's table, returns blocks.
+ *   pa_bm_num_tokens, pa_bm_num_free, pa_bm_refcount: state queries.
+ *
+ * A cached full block is identified by its own tokens and by its parent (the block before it when
+ * it was filled, and that block's content generation), so a hit is a match on the whole prefix;
+ * hits are checked token by token, so a hash collision can cost a hit but never give a wrong one.
+ * Not thread-safe: one host thread (the scheduler) owns a manager.
+ */
+#define PA_BM_DEGENERATE_HASH 1
+#define PA_BM_ERR_ARG (-1)        /* null manager / tokens, n < 1, bad block id */
+#define PA_BM_ERR_NO_BLOCKS (-2)  /* not enough free blocks: nothing changed */
+#define PA_BM_ERR_NO_SEQ (-3)     /* unknown sequence id */
+#define PA_BM_ERR_SEQ_EXISTS (-4) /* pa_bm_allocate on a live sequence id */
+typedef struct pa_block_manager pa_block_manager;
+pa_block_manager *pa_bm_create(int num_blocks, int block_size, int flags);
+void pa_bm_destroy(pa_block_manager *bm);
+int pa_bm_allocate(pa_block_manager *bm, int64_t seq, const int32_t *tokens, int n);
+int pa_bm_can_allocate(const pa_block_manager *bm, const int32_t *tokens, int n);
+int64_t pa_bm_append(pa_block_manager *bm, int64_t seq, int32_t token);
+int pa_bm_release(pa_block_manager *bm, int64_t seq);
+int pa_bm_block_table(const pa_block_manager *bm, int64_t seq, int32_t *out, int cap);
+int pa_bm_num_tokens(const pa_block_manager *bm, int64_t seq);
+int pa_bm_num_free(const pa_block_manager *bm);
+int pa_bm_refcount(const pa_block_manager *bm, int block);
+
 /* A static, human-readable name for a status code. */
 const char *pa_status_string(pa_status status);
 

@@ -18,7 +18,10 @@ LIB_PATH = PKG / "_build" / "libpagedattn.so"
 PA_F16, PA_BF16 = 0, 1
 PA_DEVERR_SLOT, PA_DEVERR_TABLE, PA_DEVERR_LENGTH = 1, 2, 4
 EXPORTS = ("pa_store_kv", "pa_decode_workspace_size", "pa_decode", "pa_store_decode",
-           "pa_prefill_varlen", "pa_decode_noalloc", "pa_status_string")
+           "pa_prefill_varlen", "pa_decode_noalloc", "pa_status_string", "pa_bm_create",
+           "pa_bm_destroy", "pa_bm_allocate", "pa_bm_can_allocate", "pa_bm_append",
+           "pa_bm_release", "pa_bm_block_table", "pa_bm_num_tokens", "pa_bm_num_free",
+           "pa_bm_refcount")
 PA_DECODE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 _lib = None
@@ -53,6 +56,27 @@ def load(path: Path | str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_prefill_varlen.restype = I
     lib.pa_decode_noalloc.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, P, P]
     lib.pa_decode_noalloc.restype = I
+    L = ctypes.c_int64
+    lib.pa_bm_create.argtypes = [I, I, I]
+    lib.pa_bm_create.restype = P
+    lib.pa_bm_destroy.argtypes = [P]
+    lib.pa_bm_destroy.restype = None
+    lib.pa_bm_allocate.argtypes = [P, L, P, I]
+    lib.pa_bm_allocate.restype = I
+    lib.pa_bm_can_allocate.argtypes = [P, P, I]
+    lib.pa_bm_can_allocate.restype = I
+    lib.pa_bm_append.argtypes = [P, L, ctypes.c_int32]
+    lib.pa_bm_append.restype = L
+    lib.pa_bm_release.argtypes = [P, L]
+    lib.pa_bm_release.restype = I
+    lib.pa_bm_block_table.argtypes = [P, L, P, I]
+    lib.pa_bm_block_table.restype = I
+    lib.pa_bm_num_tokens.argtypes = [P, L]
+    lib.pa_bm_num_tokens.restype = I
+    lib.pa_bm_num_free.argtypes = [P]
+    lib.pa_bm_num_free.restype = I
+    lib.pa_bm_refcount.argtypes = [P, I]
+    lib.pa_bm_refcount.restype = I
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -209,3 +233,78 @@ def pa_prefill_varlen(out, q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k
         _i32(cu_seqlens_q, "cu_seqlens_q"), _i32(cu_seqlens_k, "cu_seqlens_k"), S, Tq, total_k,
         int(max_seqlen_q), int(max_seqlen_k), _i32(block_tables, "block_tables"), maxb, Hq, Hkv, D,
         bs, NB, float(scale), int(bool(causal)), dt, _i32(err, "err"), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------------------------
+# host block manager
+# ---------------------------------------------------------------------------------------------
+
+PA_BM_DEGENERATE_HASH = 1
+BM_ERRORS = {-1: "bad argument", -2: "no free blocks", -3: "unknown sequence",
+             -4: "sequence already allocated"}
+
+
+class BlockManagerError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {code} ({BM_ERRORS.get(code, 'unknown')})")
+        self.code = code
+
+
+class BlockManager:
+    """The library's host block manager (include/pa.h, pa_bm_*): block ids, reference counts and
+    the exact full-block prefix cache, one block table per sequence. Marshalling only."""
+
+    def __init__(self, num_blocks: int, block_size: int, flags: int = 0):
+        self._lib = load()
+        self._h = self._lib.pa_bm_create(int(num_blocks), int(block_size), int(flags))
+        if not self._h:
+            raise BlockManagerError("pa_bm_create", -1)
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._lib.pa_bm_destroy(h)
+
+    @staticmethod
+    def _tokens(tokens):
+        import numpy as np
+        a = np.ascontiguousarray(tokens, dtype=np.int32)
+        return a, a.ctypes.data
+
+    def _ok(self, fn: str, r: int) -> int:
+        if r < 0:
+            raise BlockManagerError(fn, int(r))
+        return int(r)
+
+    def allocate(self, seq: int, tokens) -> int:
+        """Blocks for a new sequence; returns the number of its tokens already cached."""
+        a, ptr = self._tokens(tokens)
+        return self._ok("pa_bm_allocate", self._lib.pa_bm_allocate(self._h, int(seq), ptr, a.size))
+
+    def can_allocate(self, tokens) -> bool:
+        a, ptr = self._tokens(tokens)
+        return bool(self._ok("pa_bm_can_allocate", self._lib.pa_bm_can_allocate(self._h, ptr, a.size)))
+
+    def append(self, seq: int, token: int) -> int:
+        """One more token; returns its slot."""
+        return self._ok("pa_bm_append", self._lib.pa_bm_append(self._h, int(seq), int(token)))
+
+    def release(self, seq: int) -> None:
+        self._ok("pa_bm_release", self._lib.pa_bm_release(self._h, int(seq)))
+
+    def block_table(self, seq: int) -> list:
+        import numpy as np
+        n = self._ok("pa_bm_block_table", self._lib.pa_bm_block_table(self._h, int(seq), None, 0))
+        out = np.empty(max(n, 1), dtype=np.int32)
+        self._ok("pa_bm_block_table", self._lib.pa_bm_block_table(self._h, int(seq), out.ctypes.data, n))
+        return out[:n].tolist()
+
+    def num_tokens(self, seq: int) -> int:
+        return self._ok("pa_bm_num_tokens", self._lib.pa_bm_num_tokens(self._h, int(seq)))
+
+    def num_free(self) -> int:
+        return self._ok("pa_bm_num_free", self._lib.pa_bm_num_free(self._h))
+
+    def refcount(self, block: int) -> int:
+        return self._ok("pa_bm_refcount", self._lib.pa_bm_refcount(self._h, int(block)))
