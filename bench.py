@@ -94,6 +94,26 @@ def traffic_of(rec: dict):
 # distributed plumbing
 # ---------------------------------------------------------------------------------------------
 
+def rank_seed(base: int, rank: int, layer: int) -> int:
+    """Seed of one rank's layer: every rank runs its own replica on its own data."""
+    return base + 1000 * rank + layer
+
+
+def slowest(torch, value: float, dist, device) -> float:
+    """The largest value over the ranks (the slowest rank's time); the value itself alone."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_gbs(world: int, bytes_per_rank: float, elapsed_ms: float) -> float:
+    """Whole-job GB/s of `world` replicas that each moved bytes_per_rank in the slowest rank's
+    elapsed_ms."""
+    return world * bytes_per_rank / (elapsed_ms * 1e-3) / 1e9
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -264,7 +284,7 @@ def run_gpu(args, ws_, rank, local):
 
     # ---- inputs: two layers of the decode workload (seeds differ per layer and rank) ----
     base = W.CONFIGS[args.workload].seed
-    layers = [DecodeLayer(torch, pa, W.make(args.workload, seed=base + 1000 * rank + l), dev)
+    layers = [DecodeLayer(torch, pa, W.make(args.workload, seed=rank_seed(base, rank, l)), dev)
               for l in range(args.layers)]
     c0 = layers[0].c
     nbytes = [kv_bytes(L.c.context_lens, L.c.Hkv, L.c.D) for L in layers]
@@ -331,12 +351,10 @@ def run_gpu(args, ws_, rank, local):
     st_ms = [a.elapsed_time(b) for a, b, _ in st_ev]
     two_ms = [a.elapsed_time(c) for a, _, c in st_ev]
     if dist is not None:
-        tt = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed = float(tt.item())
+        elapsed = slowest(torch, elapsed, dist, dev)
     ms_step = elapsed / args.steps
     step_bytes = sum(nbytes[i % nl] for i in range(args.steps))
-    value = ws_ * step_bytes / (elapsed * 1e-3) / 1e9
+    value = weak_gbs(ws_, step_bytes, elapsed)
     dec_mean = statistics.mean(dec_ms)
     dec_bytes_mean = statistics.mean(nbytes[i % nl] for i in range(args.steps))
     achieved = dec_bytes_mean / (dec_mean * 1e-3) / 1e9
@@ -383,10 +401,8 @@ def run_gpu(args, ws_, rank, local):
     torch.cuda.synchronize()
     e_ms = e0.elapsed_time(e1)
     if dist is not None:
-        tt = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e_ms = float(tt.item())
-    e2e_value = ws_ * nbytes[0] * e_steps / (e_ms * 1e-3) / 1e9 if e_steps else None
+        e_ms = slowest(torch, e_ms, dist, dev)
+    e2e_value = weak_gbs(ws_, nbytes[0] * e_steps, e_ms) if e_steps else None
 
     # ---- other rows: prefill with a cached prefix (store + varlen prefill) ----
     rows = {}
