@@ -18,7 +18,7 @@
 //    share a block) into a ring of shared-memory stages, plus a bulk copy of the G query rows at
 //    the start of each segment. full/empty mbarriers hand stages to and from the consumers; the
 //    ring (2-6 stages of 32-64 KB) keeps up to ~130 KB per SM in flight across pair boundaries.
-//  * Consumers: warp w owns rows 16w..16w+15 of every 128-row tile. QK: LPP lanes per row, each holding E
+//  * Consumers, small groups (G <= 3): warp w owns rows 8w..8w+7 of every 64-row tile. QK: LPP lanes per row, each holding E
 //    query elements per head (scaled by scale*log2 e) and multiplying with packed fp32 pairs
 //    (two independent passes of 8 rows);
 //    the chunk each lane reads depends on the lane so that rows sharing a bank phase hit
@@ -26,6 +26,14 @@
 //    owning 8 output columns. At a segment's end the 8 warps' (max, sum, O) are combined: a
 //    segment covering its whole pair writes the output; a partial segment writes (O/sum, max,
 //    sum) to one of the CTA's two workspace slots, and decode_merge_kernel combines the pieces.
+//  * Consumers, large groups (G >= 4): at ~G multiply-adds per byte the fp32 pipes, not HBM,
+//    would set the pace, so the G heads of one KV head go through the warp-level tensor-core
+//    path as the M rows of a 16-row fragment (heads G..15 are zero). Per warp and tile:
+//    S[16 x 8 rows] = Q K^T with m16n8k16 over D, the online softmax on the score fragment
+//    (a quad of lanes holds one head's 8 scores), then O[16 x D] += P V with m16n8k8, P taken
+//    straight from the score fragment and the V fragments read transposed by ldmatrix. The K/V
+//    tiles land through TMA with the 128-byte swizzle (two 64-column halves when D = 128) so
+//    the ldmatrix reads are free of bank conflicts.
 //  * Every wait is bounded (PA_DEVERR_TIMEOUT); the producer drains its copies before exiting.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -40,14 +48,35 @@ namespace {
 constexpr int kTN = 64;                  // positions per tile
 constexpr int kConsumers = 8;            // consumer warps
 constexpr int kWPos = kTN / kConsumers;  // rows per consumer warp per tile
-constexpr int kThreads = 32 * (1 + kConsumers);
 constexpr int kConsThreads = 32 * kConsumers;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kSmemPerSm = 227 * 1024;
-// persistent CTAs per SM: two (two TMA streams, 16 consumer warps) when the group is small
-// enough for the halved register file, else one
+constexpr int kMaxStages = 8;  // the tile metas and barriers of 8 stages fit their 1 KB
+constexpr int kLaneBoxes = (kTN + 31) / 32;  // TMA boxes per producer lane and tile, at most
+constexpr int kLook = 2;                     // a producer's steps prepared ahead of the one it issues
+constexpr int kIdRing = 4;                   // each producer's ring of prepared tiles (> kLook)
+static_assert(kIdRing > kLook && (kIdRing & (kIdRing - 1)) == 0, "block-id ring");
+
+struct PrepTile {
+    int b, g, t, n, nt, pad[3];
+};
+// tensor-core consumers from this group size on
+constexpr int kMmaMinGroup = 4;
 template <int G>
-constexpr int ctas_per_sm() { return G <= 3 ? 2 : 1; }
+constexpr bool use_mma() { return G >= kMmaMinGroup; }
+// persistent CTAs per SM: two (two TMA streams, 16 consumer warps) when the consumers fit the
+// halved register file, else one
+__host__ __device__ constexpr int ctas_per_sm(int D, int G) { return G < kMmaMinGroup ? 2 : 1; }
+// producer warps (alternate tiles): two keep the light tensor-core consumers fed; with the fp32
+// consumers one suffices and a second only takes issue slots from them
+__host__ __device__ constexpr int producers_for(int G) { return G < kMmaMinGroup ? 1 : 2; }
+__host__ __device__ constexpr int threads_for(int G) { return 32 * (producers_for(G) + kConsumers); }
+// one swizzled tile half: 64 rows + the spare row of 128 bytes. The 128-byte swizzle is a
+// function of the shared-memory address (16-byte chunk c of the 128-byte line at address a sits
+// at c ^ ((a >> 7) & 7)), so halves need only 128-byte alignment and readers take the phase from
+// the address.
+constexpr int kSwRows = kTN + 1;
+constexpr int kSwHalf = kSwRows * 128;
 
 // flags of one tile
 constexpr int kFirst = 1;  // first tile of a segment: reset the state, read q
@@ -87,7 +116,7 @@ struct DecodeParams {
 template <int D, int G>
 struct Shape {
     static constexpr int NCH = D / 8;  // 16-byte chunks per row
-    static constexpr int CPS = ctas_per_sm<G>();
+    static constexpr int CPS = ctas_per_sm(D, G);
     // QK elements per lane: keeps the query registers (G * E) at 32 with two CTAs per SM,
     // at 64 with one
     static constexpr int E_RAW = CPS == 2 ? (G == 1 ? 32 : G == 2 ? 16 : 8) : (G <= 4 ? 16 : 8);
@@ -103,12 +132,18 @@ struct Shape {
     static constexpr int PV_IT = kWPos / RPI;
     static constexpr int HPR = 32 / kWPos;                    // softmax heads per round
     static constexpr int ROUNDS = (G + HPR - 1) / HPR;
-    // 64 rows + a spare row that takes a new token's K (or V) row in the fused store + decode
-    static constexpr int TILE_BYTES = (kTN + 1) * D * 2;
+    static constexpr bool MMA = use_mma<G>();
+    static constexpr int NH = D / 64;  // 64-column halves of a swizzled tile
+    // 64 rows + a spare row that takes a new token's K (or V) row in the fused store + decode;
+    // tensor-core consumers: NH swizzled halves of 128-byte rows
+    static constexpr int TILE_BYTES = MMA ? NH * kSwHalf : (kTN + 1) * D * 2;
     static constexpr int Q_BYTES = G * D * 2;
-    static constexpr int STAGE_BYTES = (2 * TILE_BYTES + Q_BYTES + 1023) / 1024 * 1024;
+    // stages on 1 KB boundaries for the unswizzled tiles; 128 bytes suffice for the swizzled ones
+    static constexpr int STAGE_ALIGN = MMA ? 128 : 1024;
+    static constexpr int STAGE_BYTES = (2 * TILE_BYTES + Q_BYTES + STAGE_ALIGN - 1) / STAGE_ALIGN * STAGE_ALIGN;
     static constexpr int RED_BYTES = kConsumers * G * (D + 2) * 4;
-    static constexpr int SCRATCH_BYTES = 2 * kConsumers * G * kWPos * 4 + kConsumers * G * 4;
+    // scores, probabilities and rescale factors of the fp32 consumers
+    static constexpr int SCRATCH_BYTES = MMA ? 0 : 2 * kConsumers * G * kWPos * 4 + kConsumers * G * 4;
     static_assert(PASSES >= 1 && PPP * PASSES == kWPos, "QK mapping");
     static_assert(RPI * PV_IT == kWPos, "PV mapping");
     // chunk that lane (row u of a pass, part r) reads at step c. With 4 lanes per row two rows
@@ -121,8 +156,9 @@ struct Shape {
 
 template <int D, int G>
 constexpr int fixed_smem() {
-    // + metas, barriers, scan scratch (1 KB) and the slack that aligns the ring (1 KB)
-    return Shape<D, G>::RED_BYTES + Shape<D, G>::SCRATCH_BYTES + 2048;
+    // + metas, barriers, scan scratch (1 KB), the slack that aligns the ring (1 KB) and the
+    // producer's ring of prepared tiles
+    return Shape<D, G>::RED_BYTES + Shape<D, G>::SCRATCH_BYTES + 2048 + producers_for(G) * kIdRing * (kTN * 4 + 32);
 }
 
 // All 32 lanes wait for the phase, then the warp reconverges; false (for every lane) if the wait
@@ -141,27 +177,71 @@ __device__ __forceinline__ unsigned warp_rows_valid(const TileMeta &m, int cw) {
     return static_cast<unsigned>(w >> (first & 63)) & ((1u << kWPos) - 1u);
 }
 
+// ldmatrix: four 8x8 matrices of 16-bit elements; lane 8j + i gives the address of row i of
+// matrix j, and register j of lane l holds (row l / 4, columns 2 (l % 4), +1) of matrix j
+// (transposed: rows 2 (l % 4), +1 of column l / 4)
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// d += A B with A 16 x 16 (row-major fragment; rows 8..15 zero, so only a0 and a2 are passed)
+// and B 16 x 8, fp32 accumulation
+template <class E>
+__device__ __forceinline__ void mma_k16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    if constexpr (E::kIsBf16)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+// d += A B with A 16 x 8 and B 8 x 8
+template <class E>
+__device__ __forceinline__ void mma_k8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    if constexpr (E::kIsBf16)
+        asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(b0));
+    else
+        asm("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(b0));
+}
+
 __device__ __forceinline__ int ntiles_of(const DecodeParams &p, int b, long long cap) {
     const int n = p.context_lens[b];
     if (n <= 0 || n > cap) return 0;
     return (n + kTN - 1) / kTN;
 }
 
-// block-wide sum over all kThreads threads; `red` holds kThreads / 32 longs
+// block-wide sum over all NT threads; `red` holds NT / 32 longs
+template <int NT>
 __device__ long long block_sum(long long v, long long *red) {
     for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
     const int w = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) red[w] = v;
     __syncthreads();
     long long t = 0;
-    for (int i = 0; i < kThreads / 32; ++i) t += red[i];
+    for (int i = 0; i < NT / 32; ++i) t += red[i];
     __syncthreads();
     return t;
 }
 
 template <int D, int G, class E>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(threads_for(G), ctas_per_sm(D, G)) decode_kernel(const __grid_constant__ DecodeParams p) {
     using S = Shape<D, G>;
+    constexpr int kProducers = producers_for(G), kThreads = threads_for(G);
     using T = typename E::T;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // stages start on a 1024-byte boundary (the launch adds 1 KB of slack for this)
@@ -172,10 +252,12 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
     float *sbuf = red + kConsumers * G * (D + 2);                        // [8][G][16] scores
     float *pbuf = sbuf + kConsumers * G * kWPos;                         // [8][G][16] probs
     float *abuf = pbuf + kConsumers * G * kWPos;                         // [8][G] rescale
-    TileMeta *metas = reinterpret_cast<TileMeta *>(abuf + kConsumers * G);
+    TileMeta *metas = reinterpret_cast<TileMeta *>(reinterpret_cast<unsigned char *>(sbuf) + S::SCRATCH_BYTES);
     uint64_t *bars = reinterpret_cast<uint64_t *>(metas + NS);  // full[NS], empty[NS], cons[2]
     long long *scan = reinterpret_cast<long long *>(bars + 2 * NS + 2);  // 16 longs + start
     volatile int *abort_flag = reinterpret_cast<volatile int *>(scan + 20);
+    PrepTile *prep = reinterpret_cast<PrepTile *>(scan + 24);  // [producers][kIdRing]
+    int *idring = reinterpret_cast<int *>(prep + kProducers * kIdRing);  // [producers][kIdRing][kTN]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = gridDim.x, cta = blockIdx.x;
@@ -208,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
             for (int i = 0; i < p.Hq * D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
         }
     }
-    const long long total = block_sum(mine, scan) * p.Hkv;
+    const long long total = block_sum<kThreads>(mine, scan) * p.Hkv;
     const long long lo = total * cta / P, hi = total * (cta + 1) / P;
 
     // ---- pass 2: the (b, g, t) of tile `lo` ----
@@ -264,34 +346,28 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
     if (lo >= hi || b0 < 0) return;
     const long long count = hi - lo;
 
-    if (warp == 0) {
-        // ======================= producer =======================
-        prefetch_tmap(&p.tmap_k);
-        prefetch_tmap(&p.tmap_v);
+    if (warp < kProducers) {
+        // ======================= producers =======================
+        // producer pw issues tiles i = pw, pw + kProducers, ... (stage i % NS: with NS a multiple
+        // of kProducers every stage has one producer)
+        const int pw = warp;
+        if (lane == 0) {
+            prefetch_tmap(&p.tmap_k);
+            prefetch_tmap(&p.tmap_v);
+        }
         const int R = p.box_rows, nbox = kTN / R;
         const uint32_t box_bytes = static_cast<uint32_t>(R) * D * 2;
+        const unsigned long long box_rows_mask = R == 64 ? ~0ull : ((1ull << R) - 1ull);
         // walker: the next tile to prepare
         int b = b0;
         int nt = ntiles_of(p, b, cap);
         int n = p.context_lens[b];
-        long long off = lo - seq_start;
+        const long long off = lo - seq_start;
         int g = static_cast<int>(off / nt), t = static_cast<int>(off % nt);
-        // the prepared tile: its coordinates and the block ids of this lane's boxes (lane l takes
-        // boxes l, l + 32, l + 64, l + 96). Preparing tile i+1 right after issuing tile i puts the
-        // block-table loads in flight while the producer waits for a free stage.
-        int pb_ = 0, pg = 0, pt = 0, pn = 0, pnt = 0, pid[4];
-        auto prepare = [&]() {
-            pb_ = b; pg = g; pt = t; pn = n; pnt = nt;
-            const int pos0 = t * kTN;
-            const int nvalid = min(kTN, n - pos0);
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const int k = lane + 32 * k4;
-                pid[k4] = -2;  // no box
-                if (k < nbox && k * R < nvalid)
-                    pid[k4] = p.block_tables[static_cast<size_t>(b) * p.max_blocks +
-                                             p.geom.block_of(pos0 + k * R)];
-            }
+        // the CTA's first segment: tiles [0, first_len); it began inside its pair if t > 0
+        const long long first_len = min(count, static_cast<long long>(nt - t));
+        const bool first_mid = t > 0;
+        auto advance = [&]() {
             if (++t == nt) {
                 t = 0;
                 if (++g == p.Hkv) {
@@ -303,14 +379,98 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
                 }
             }
         };
-        prepare();
-        int seg_t0 = 0;  // first tile of the current segment within its pair
-        bool first_seg = true;
-        long long issued = 0;
-        int stage = 0;
-        uint32_t phase = 0;
-        for (long long i = 0; i < count; ++i) {
+        for (int k = 0; k < pw && k < count; ++k) advance();
+        PrepTile *myprep = prep + pw * kIdRing;
+        int *myids = idring + pw * kIdRing * kTN;
+        // Each producer prepares its tiles kLook of its own steps ahead of the one it issues:
+        // preparing records the tile's coordinates and queues cp.async copies of its block ids
+        // (lane l: boxes l and l + 32) into a ring in shared memory, so the block-table reads are
+        // in flight while earlier tiles are issued. Every step commits one cp.async group per lane.
+        auto prepare = [&](long long j) {
+            const int sl = static_cast<int>(j % kIdRing);
+            if (lane == 0) myprep[sl] = PrepTile{b, g, t, n, nt};
+            const int pos0 = t * kTN;
+            const int nvalid = min(kTN, n - pos0);
+#pragma unroll
+            for (int k2 = 0; k2 < kLaneBoxes; ++k2) {
+                const int k = lane + 32 * k2;
+                if (k < nbox && k * R < nvalid)
+                    cp_async4(smem_addr(myids + sl * kTN + k),
+                              p.block_tables + static_cast<size_t>(b) * p.max_blocks + p.geom.block_of(pos0 + k * R));
+            }
+            cp_async_commit();
+#pragma unroll
+            for (int k = 0; k < kProducers; ++k) advance();
+        };
+        const long long my_count = count > pw ? (count - pw + kProducers - 1) / kProducers : 0;
+        for (int j = 0; j < kLook; ++j) {
+            if (j < my_count) prepare(j);
+            else cp_async_commit();
+        }
+        long long last_i = -1;  // the last tile this producer issued
+        for (long long j = 0; j < my_count; ++j) {
+            const long long i = pw + static_cast<long long>(kProducers) * j;
             if (__shfl_sync(kFull, lane == 0 ? *abort_flag : 0, 0)) break;  // warp-uniform
+            if (j + kLook < my_count) prepare(j + kLook);
+            else cp_async_commit();
+            const int stage = static_cast<int>(i % NS);
+            const uint32_t phase = static_cast<uint32_t>((i / NS) & 1);
+            // everything up to the copies is worked out before the stage is free
+            cp_async_wait<kLook>();  // this lane's block ids of tile i have landed
+            __syncwarp();
+            const int sl = static_cast<int>(j % kIdRing);
+            const PrepTile pm = myprep[sl];
+            const int pb_ = pm.b, pg = pm.g, pt = pm.t, pn = pm.n, pnt = pm.nt;
+            const int pos0 = pt * kTN;
+            const int nvalid = min(kTN, pn - pos0);
+            int slots[kLaneBoxes];
+            unsigned good[kLaneBoxes], badm[kLaneBoxes];
+#pragma unroll
+            for (int k2 = 0; k2 < kLaneBoxes; ++k2) {
+                const int k = lane + 32 * k2;
+                slots[k2] = -1;
+                bool bad = false;
+                if (k < nbox && k * R < nvalid) {
+                    const int id = myids[sl * kTN + k];
+                    if (id >= 0 && id < p.num_blocks)
+                        slots[k2] = id * p.geom.block_size + p.geom.offset_of(pos0 + k * R);
+                    else
+                        bad = true;
+                }
+                good[k2] = __ballot_sync(kFull, slots[k2] >= 0);
+                badm[k2] = __ballot_sync(kFull, bad);
+            }
+            // rows holding context positions: [0, nvalid), minus the boxes of ids outside the pool
+            unsigned long long vmask = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+            unsigned nbad = 0, ngood = 0;
+#pragma unroll
+            for (int k2 = 0; k2 < kLaneBoxes; ++k2) {
+                nbad += __popc(badm[k2]);
+                ngood += __popc(good[k2]);
+            }
+            if (nbad) {  // rare: flagged, and those rows are masked
+                if (lane == 0) raise_err(p.err, PA_DEVERR_TABLE);
+#pragma unroll
+                for (int k2 = 0; k2 < kLaneBoxes; ++k2)
+                    for (unsigned m = badm[k2]; m; m &= m - 1) {
+                        const int k = 32 * k2 + __ffs(m) - 1;
+                        vmask &= ~(box_rows_mask << (k * R));
+                    }
+            }
+            uint32_t bytes = ngood * 2u * box_bytes;
+            const bool last = (i == count - 1) || (pt == pnt - 1);
+            const bool first = (i == 0) || (pt == 0);
+            const bool in_first = i < first_len;  // the CTA's first segment
+            int flags = (first ? kFirst : 0) | (last ? kLast : 0);
+            // the segment covers its whole pair: it ends the pair and began at the pair's start
+            if (last && pt == pnt - 1 && !(in_first && first_mid)) flags |= kWhole;
+            if (!in_first) flags |= kSlot1;
+            if (first) bytes += S::Q_BYTES;
+            // fused store: the pair's last tile holds the new token (position pn - 1); its rows
+            // come from k_new / v_new into the spare rows, not from the pool
+            const bool new_tok = p.k_new != nullptr && pt == pnt - 1;
+            if (new_tok) bytes += 2 * D * 2;
+
             // every lane waits and the warp reconverges before going on (a lane-0-only wait
             // leaves the warp split for the rest of the iteration)
             const bool ok = warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag);
@@ -321,57 +481,15 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
                 }
                 break;
             }
-            const int pos0 = pt * kTN;
-            const int nvalid = min(kTN, pn - pos0);
-            int slots[4];
-            unsigned long long vm[2] = {0ull, 0ull};
-            uint32_t bytes = 0;
-#pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const int k = lane + 32 * k4;
-                slots[k4] = -1;
-                if (pid[k4] == -2) continue;
-                if (pid[k4] >= 0 && pid[k4] < p.num_blocks) {
-                    slots[k4] = pid[k4] * p.geom.block_size + p.geom.offset_of(pos0 + k * R);
-                    const int r0 = k * R, r1 = r0 + min(R, nvalid - r0);  // rows [r0, r1)
-#pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        const int a = max(r0, 64 * w), e = min(r1, 64 * w + 64);
-                        if (a < e)
-                            vm[w] |= (e - a == 64 ? ~0ull : ((1ull << (e - a)) - 1)) << (a - 64 * w);
-                    }
-                    bytes += 2 * box_bytes;
-                } else {
-                    raise_err(p.err, PA_DEVERR_TABLE);
-                }
-            }
-            unsigned vw[4];
-            vw[0] = __reduce_or_sync(kFull, static_cast<unsigned>(vm[0]));
-            vw[1] = __reduce_or_sync(kFull, static_cast<unsigned>(vm[0] >> 32));
-            vw[2] = __reduce_or_sync(kFull, static_cast<unsigned>(vm[1]));
-            vw[3] = __reduce_or_sync(kFull, static_cast<unsigned>(vm[1] >> 32));
-            bytes = __reduce_add_sync(kFull, bytes);
-            const bool last = (i == count - 1) || (pt == pnt - 1);
-            const bool first = (i == 0) || (pt == 0);
-            if (first) seg_t0 = pt;
-            int flags = (first ? kFirst : 0) | (last ? kLast : 0);
-            if (last && seg_t0 == 0 && pt == pnt - 1) flags |= kWhole;
-            if (!first_seg) flags |= kSlot1;
-            if (first) bytes += S::Q_BYTES;
-            // fused store: the pair's last tile holds the new token (position pn - 1); its rows
-            // come from k_new / v_new into the spare rows, not from the pool
-            const bool new_tok = p.k_new != nullptr && pt == pnt - 1;
-            if (new_tok) bytes += 2 * D * 2;
-
             unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
             if (lane == 0) {
                 TileMeta m;
                 m.b = pb_;
                 m.g = pg;
                 m.flags = flags;
-                m.all_valid = (vw[0] & vw[1] & vw[2] & vw[3]) == 0xffffffffu;
-                m.valid[0] = (static_cast<unsigned long long>(vw[1]) << 32) | vw[0];
-                m.valid[1] = (static_cast<unsigned long long>(vw[3]) << 32) | vw[2];
+                m.all_valid = vmask == ~0ull;
+                m.valid[0] = vmask;
+                m.valid[1] = 0ull;
                 m.newrow = new_tok ? (pn - 1) - pos0 : -1;
                 m.pad = 0;
                 metas[stage] = m;
@@ -380,11 +498,21 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
             __syncwarp();
             const uint32_t kdst = smem_addr(st), vdst = kdst + S::TILE_BYTES;
 #pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const int k = lane + 32 * k4;
-                if (slots[k4] >= 0) {
-                    tma_load_3d(kdst + k * box_bytes, &p.tmap_k, 0, pg, slots[k4], full0 + 8 * stage);
-                    tma_load_3d(vdst + k * box_bytes, &p.tmap_v, 0, pg, slots[k4], full0 + 8 * stage);
+            for (int k2 = 0; k2 < kLaneBoxes; ++k2) {
+                const int k = lane + 32 * k2;
+                if (slots[k2] >= 0) {
+                    if constexpr (S::MMA) {
+                        // one box per 64-column half, 128-byte rows, swizzled
+#pragma unroll
+                        for (int hf = 0; hf < S::NH; ++hf) {
+                            const uint32_t o = hf * kSwHalf + k * R * 128;
+                            tma_load_3d(kdst + o, &p.tmap_k, 64 * hf, pg, slots[k2], full0 + 8 * stage);
+                            tma_load_3d(vdst + o, &p.tmap_v, 64 * hf, pg, slots[k2], full0 + 8 * stage);
+                        }
+                    } else {
+                        tma_load_3d(kdst + k * box_bytes, &p.tmap_k, 0, pg, slots[k2], full0 + 8 * stage);
+                        tma_load_3d(vdst + k * box_bytes, &p.tmap_v, 0, pg, slots[k2], full0 + 8 * stage);
+                    }
                 }
             }
             if (first && lane == 0) {
@@ -394,14 +522,26 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
             if (new_tok) {
                 const size_t row_off = (static_cast<size_t>(pb_) * p.Hkv + pg) * D;
                 if (lane == 0) {
-                    bulk_load(kdst + kTN * D * 2, static_cast<const T *>(p.k_new) + row_off, D * 2,
-                              full0 + 8 * stage);
-                    bulk_load(vdst + kTN * D * 2, static_cast<const T *>(p.v_new) + row_off, D * 2,
-                              full0 + 8 * stage);
+                    if constexpr (S::MMA) {
+                        // row kTN of each half, copied in as it is (readers take phase 0 there)
+#pragma unroll
+                        for (int hf = 0; hf < S::NH; ++hf) {
+                            const uint32_t o = hf * kSwHalf + kTN * 128;
+                            bulk_load(kdst + o, static_cast<const T *>(p.k_new) + row_off + 64 * hf, 128,
+                                      full0 + 8 * stage);
+                            bulk_load(vdst + o, static_cast<const T *>(p.v_new) + row_off + 64 * hf, 128,
+                                      full0 + 8 * stage);
+                        }
+                    } else {
+                        bulk_load(kdst + kTN * D * 2, static_cast<const T *>(p.k_new) + row_off, D * 2,
+                                  full0 + 8 * stage);
+                        bulk_load(vdst + kTN * D * 2, static_cast<const T *>(p.v_new) + row_off, D * 2,
+                                  full0 + 8 * stage);
+                    }
                 }
                 // ... and into the pool, at the slot of position pn - 1 (no copy in this launch
                 // reads that slot's row: the tile takes it from the spare row)
-                const int id = p.block_tables[static_cast<size_t>(pb_) * p.max_blocks + p.geom.block_of(pn - 1)];
+                const int id = myids[sl * kTN + (pn - 1 - pos0) / R];  // its box's block
                 constexpr int kChunks = D * 2 / 16;  // 16-byte chunks per row
                 if (id >= 0 && id < p.num_blocks && lane < 2 * kChunks) {
                     const long long slot = static_cast<long long>(id) * p.geom.block_size + p.geom.offset_of(pn - 1);
@@ -414,18 +554,13 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
                     *dst = *src;
                 }
             }
-            ++issued;
-            if (last) first_seg = false;
-            if (++stage == NS) {
-                stage = 0;
-                phase ^= 1;
-            }
-            if (i + 1 < count) prepare();
+            last_i = i;
         }
-        // no copy may still be in flight when the CTA exits
-        if (lane == 0) {
-            const long long from = issued > NS ? issued - NS : 0;
-            for (long long i = from; i < issued; ++i) {
+        // no copy (TMA or block id) may still be in flight when the CTA exits: wait for the
+        // tiles this producer issued in the last NS tiles
+        cp_async_wait<0>();
+        if (lane == 0 && last_i >= 0) {
+            for (long long i = last_i; i >= 0 && i > last_i - NS; i -= kProducers) {
                 if (!mbar_wait(full0 + 8 * static_cast<int>(i % NS), static_cast<uint32_t>((i / NS) & 1))) {
                     raise_err(p.err, PA_DEVERR_TIMEOUT);
                     *abort_flag = 1;
@@ -437,220 +572,21 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
     }
 
     // ========================= consumers =========================
-    const int cw = warp - 1;  // 0..7
-    const int r = lane % S::LPP;
-    const int rg = lane / S::LPR, cc = lane % S::LPR;
-    // softmax: lane handles row spos of heads shead + HPR * k (HPR = 32 / rows per warp)
-    const int spos = lane % kWPos, shead = lane / kWPos;
-    float *sb = sbuf + cw * G * kWPos;
-    float *pb = pbuf + cw * G * kWPos;
-    float *ab = abuf + cw * G;
-
-    uint64_t q2[G][S::CPL][4];
-    uint64_t acc[G][S::NPV];
-    float m_run[S::ROUNDS], l_part[S::ROUNDS];
-    int seg = 0;  // segments finished (parity of the consumer barriers)
-    int stage = 0;
-    uint32_t phase = 0;
-
-    for (long long i = 0; i < count; ++i) {
-        bool ok = warp_wait(full0 + 8 * stage, phase, abort_flag);
-        if (!ok) {
-            if (lane == 0) {
-                raise_err(p.err, PA_DEVERR_TIMEOUT);
-                *abort_flag = 1;
-            }
-            return;
-        }
-        const TileMeta &m = metas[stage];
-        const int mflags = m.flags, mb = m.b, mg = m.g, mall = m.all_valid, mnew = m.newrow;
-        const unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
-        const uint32_t kb = smem_addr(st), vb = kb + S::TILE_BYTES;
-        // this warp's rows as a validity mask (bit rl: row rl of the warp)
-        const unsigned vrows = warp_rows_valid(m, cw);
-
-        if (mflags & kFirst) {
-            const T *qs = reinterpret_cast<const T *>(st + 2 * S::TILE_BYTES);
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int c = 0; c < S::CPL; ++c) {
-                    const int j = S::chunk(c, r, (lane / S::LPP));
-                    const uint4 u = *reinterpret_cast<const uint4 *>(qs + h * D + j * 8);
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = E::unpack2(w[e]);
-                        q2[h][c][e] = f2_pack(f.x * p.scale_log2, f.y * p.scale_log2);
-                    }
-                }
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < S::NPV; ++e) acc[h][e] = 0;
-#pragma unroll
-            for (int k = 0; k < S::ROUNDS; ++k) {
-                m_run[k] = -INFINITY;
-                l_part[k] = 0.f;
-            }
-        }
-
-        // ---- scores of this warp's 16 rows ----
-#pragma unroll
-        for (int pass = 0; pass < S::PASSES; ++pass) {
-            const int u = lane / S::LPP;
-            const int rl = pass * S::PPP + u;  // row within the warp's 16
-            const int row = cw * kWPos + rl;
-            uint64_t d2[G][S::CPL];
-#pragma unroll
-            for (int c = 0; c < S::CPL; ++c) {
-                const uint4 kv = lds128(kb + (row == mnew ? kTN : row) * D * 2 + S::chunk(c, r, u) * 16);
-                const uint64_t k0 = unpack_pair<E>(kv.x), k1 = unpack_pair<E>(kv.y);
-                const uint64_t k2 = unpack_pair<E>(kv.z), k3 = unpack_pair<E>(kv.w);
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    uint64_t a = f2_mul(q2[h][c][0], k0);
-                    a = f2_fma(q2[h][c][1], k1, a);
-                    a = f2_fma(q2[h][c][2], k2, a);
-                    d2[h][c] = f2_fma(q2[h][c][3], k3, a);
-                }
-            }
-            float dot[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                // pairwise tree over the chunks keeps the dependency chain short
-                uint64_t t2 = d2[h][0];
-#pragma unroll
-                for (int c = 1; c < S::CPL; ++c) t2 = f2_add(t2, d2[h][c]);
-                dot[h] = f2_lo(t2) + f2_hi(t2);
-            }
-#pragma unroll
-            for (int o = S::LPP / 2; o >= 1; o >>= 1)
-#pragma unroll
-                for (int h = 0; h < G; ++h) dot[h] += __shfl_xor_sync(kFull, dot[h], o);
-            if (r == 0) {
-                const bool valid = (vrows >> rl) & 1u;
-#pragma unroll
-                for (int h = 0; h < G; ++h) sb[h * kWPos + rl] = valid ? dot[h] : -INFINITY;
-            }
-        }
-        __syncwarp();
-
-        // ---- online softmax over the 16 rows ----
-#pragma unroll
-        for (int k = 0; k < S::ROUNDS; ++k) {
-            const int h = shead + S::HPR * k;
-            const bool act = h < G;
-            const float s = act ? sb[h * kWPos + spos] : -INFINITY;
-            float mt = s;
-#pragma unroll
-            for (int o = kWPos / 2; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, o));
-            const float m_new = fmaxf(m_run[k], mt);
-            const float mu = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = fast_exp2(m_run[k] - mu);
-            m_run[k] = m_new;
-            const float pr = fast_exp2(s - mu);
-            l_part[k] = fmaf(l_part[k], alpha, pr);
-            if (act) {
-                pb[h * kWPos + spos] = pr;
-                if (spos == 0) ab[h] = alpha;
-            }
-        }
-        __syncwarp();
-
-        // ---- O = alpha O + P V ----
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float al = ab[h];
-            const uint64_t a2 = f2_pack(al, al);
-#pragma unroll
-            for (int e = 0; e < S::NPV; ++e) acc[h][e] = f2_mul(acc[h][e], a2);
-        }
-        auto pv_row = [&](int rl) {
-            const int row0 = cw * kWPos + rl;
-            const int row = row0 == mnew ? kTN : row0;
-            uint64_t v[S::NPV];
-            if constexpr (S::CPV == 8) {
-                const uint4 vv = lds128(vb + row * D * 2 + cc * 16);
-                v[0] = unpack_pair<E>(vv.x);
-                v[1] = unpack_pair<E>(vv.y);
-                v[2] = unpack_pair<E>(vv.z);
-                v[3] = unpack_pair<E>(vv.w);
-            } else {
-                const uint2 vv = lds64(vb + row * D * 2 + cc * 8);
-                v[0] = unpack_pair<E>(vv.x);
-                v[1] = unpack_pair<E>(vv.y);
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float pr = pb[h * kWPos + rl];
-                const uint64_t p2 = f2_pack(pr, pr);
-#pragma unroll
-                for (int e = 0; e < S::NPV; ++e) acc[h][e] = f2_fma(p2, v[e], acc[h][e]);
-            }
-        };
-        if (mall) {
-#pragma unroll
-            for (int it = 0; it < S::PV_IT; ++it) pv_row(it * S::RPI + rg);
-        } else {
-            // rows outside the context are skipped: their stage bytes may hold anything
-#pragma unroll
-            for (int it = 0; it < S::PV_IT; ++it) {
-                const int rl = it * S::RPI + rg;
-                if ((vrows >> rl) & 1u) pv_row(rl);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + 8 * stage);
-        if (++stage == NS) {
-            stage = 0;
-            phase ^= 1;
-        }
-
-        if (!(mflags & kLast)) continue;
-
-        // ---- end of a segment: combine the 8 warps ----
-        float *ro = red + cw * G * (D + 2);
-#pragma unroll
-        for (int k = 0; k < S::ROUNDS; ++k) {
-            float l = l_part[k];
-#pragma unroll
-            for (int o = kWPos / 2; o >= 1; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
-            const int h = shead + S::HPR * k;
-            if (h < G && spos == 0) {
-                ro[h * (D + 2) + D] = m_run[k];
-                ro[h * (D + 2) + D + 1] = l;
-            }
-        }
-#pragma unroll
-        for (int o = S::LPR; o < 32; o <<= 1)
-#pragma unroll
-            for (int h = 0; h < G; ++h)
-#pragma unroll
-                for (int e = 0; e < S::NPV; ++e) {
-                    const float lo_ = f2_lo(acc[h][e]) + __shfl_xor_sync(kFull, f2_lo(acc[h][e]), o);
-                    const float hi_ = f2_hi(acc[h][e]) + __shfl_xor_sync(kFull, f2_hi(acc[h][e]), o);
-                    acc[h][e] = f2_pack(lo_, hi_);
-                }
-        if (rg == 0)
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float *dst = ro + h * (D + 2) + cc * S::CPV;
-#pragma unroll
-                for (int e = 0; e < S::NPV; ++e) {
-                    dst[2 * e] = f2_lo(acc[h][e]);
-                    dst[2 * e + 1] = f2_hi(acc[h][e]);
-                }
-            }
+    const int cw = warp - kProducers;  // 0..7
+    int seg = 0;   // segments finished (parity of the consumer barriers)
+    // Once every consumer warp has put its (max, sum, O) of a finished segment into `red`:
+    // combine the 8 warps and write the output (a whole pair) or the CTA's partial. False if
+    // a wait ran out.
+    auto combine = [&](int mflags, int mb, int mg) -> bool {
         __syncwarp();
         if (lane == 0) mbar_arrive(cons0);
-        ok = warp_wait(cons0, seg & 1, abort_flag);
+        bool ok = warp_wait(cons0, seg & 1, abort_flag);
         if (!ok) {
             if (lane == 0) {
                 raise_err(p.err, PA_DEVERR_TIMEOUT);
                 *abort_flag = 1;
             }
-            return;
+            return false;
         }
         const int ct = cw * 32 + lane;
         const size_t bh = static_cast<size_t>(mb) * p.Hq + static_cast<size_t>(mg) * G;
@@ -688,9 +624,342 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<G>()) decode_kernel(cons
                 raise_err(p.err, PA_DEVERR_TIMEOUT);
                 *abort_flag = 1;
             }
-            return;
+            return false;
         }
         ++seg;
+        return true;
+    };
+    if constexpr (S::MMA) {
+        // ---- tensor-core consumers ----
+        constexpr int KS = D / 16;  // QK k-steps; also PV m-blocks (16 output columns each)
+        const int gq = lane >> 2, tq = lane & 3;  // fragment row (head) and column pair
+        const int lr = lane & 7, lm = lane >> 3;  // ldmatrix: row of the warp's 8, matrix index
+        uint32_t qa[KS][2];  // Q as the A fragment (rows 8..15 are zero and not held)
+        float acc[KS][4];    // O^T: lane holds columns 16i + gq, +8 of heads 2tq, 2tq + 1
+        float m_run = -INFINITY, l_part = 0.f;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (long long i = 0; i < count; ++i) {
+            const bool ok = warp_wait(full0 + 8 * stage, phase, abort_flag);
+            if (!ok) {
+                if (lane == 0) {
+                    raise_err(p.err, PA_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                return;
+            }
+            const TileMeta &m = metas[stage];
+            const int mflags = m.flags, mb = m.b, mg = m.g, mall = m.all_valid, mnew = m.newrow;
+            const unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
+            const uint32_t kb = smem_addr(st), vb = kb + S::TILE_BYTES;
+            const unsigned vrows = warp_rows_valid(m, cw);
+
+            if (mflags & kFirst) {
+                const uint32_t *qs = reinterpret_cast<const uint32_t *>(st + 2 * S::TILE_BYTES);
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    qa[ks][0] = gq < G ? qs[gq * (D / 2) + 8 * ks + tq] : 0u;
+                    qa[ks][1] = gq < G ? qs[gq * (D / 2) + 8 * ks + 4 + tq] : 0u;
+                }
+#pragma unroll
+                for (int j = 0; j < KS; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+                m_run = -INFINITY;
+                l_part = 0.f;
+            }
+            // the row this lane addresses in ldmatrix: row lr of the warp's 8, or the spare row
+            // that holds the new token (copied in unswizzled: phase 0)
+            const int row0 = cw * kWPos + lr;
+            const int row = row0 == mnew ? kTN : row0;
+            const uint32_t rbase = static_cast<uint32_t>(row) * 128u;
+            const bool spare = row == kTN;
+            // 128-byte swizzle phase of this row in each half of K and V: (address >> 7) & 7
+            auto swz = [&](uint32_t a) -> uint32_t { return spare ? 0u : ((a >> 7) & 7u); };
+
+            // ---- S = Q K^T: this lane gets head gq at the warp's rows 2tq, 2tq + 1 ----
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {  // chunks 4q .. 4q + 3 (columns 32q .. 32q + 31)
+                uint32_t r4[4];
+                const uint32_t a = kb + (q >> 1) * kSwHalf + rbase;
+                ldsm_x4(a + (((4u * (q & 1) + lm) ^ swz(a)) << 4), r4);
+                mma_k16<E>(s0, qa[2 * q][0], qa[2 * q][1], r4[0], r4[1]);
+                mma_k16<E>(s1, qa[2 * q + 1][0], qa[2 * q + 1][1], r4[2], r4[3]);
+            }
+            const bool v0 = (vrows >> (2 * tq)) & 1u, v1 = (vrows >> (2 * tq + 1)) & 1u;
+            const float x0 = v0 ? (s0[0] + s1[0]) * p.scale_log2 : -INFINITY;
+            const float x1 = v1 ? (s0[1] + s1[1]) * p.scale_log2 : -INFINITY;
+
+            // ---- online softmax (base 2) over the warp's 8 rows: a quad holds one head ----
+            float mt = fmaxf(x0, x1);
+            mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+            mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+            const float m_new = fmaxf(m_run, mt);
+            const float mu = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = fast_exp2(m_run - mu);
+            const float p0 = fast_exp2(x0 - mu), p1 = fast_exp2(x1 - mu);
+            m_run = m_new;
+            l_part = fmaf(l_part, alpha, p0 + p1);
+            // P^T as the B fragment of O^T += V^T P^T: the score fragment's layout as it stands
+            const uint32_t pb = E::pack2(p0, p1);
+            // the rescale factors of this lane's two O^T columns (heads 2tq, 2tq + 1)
+            const float al0 = __shfl_sync(kFull, alpha, 8 * tq), al1 = __shfl_sync(kFull, alpha, 8 * tq + 4);
+
+            // ---- O^T = alpha O^T + V^T P^T, V^T read transposed by ldmatrix; rows outside the
+            // context are zeroed in the V fragment (their stage bytes may hold anything, and
+            // 0 * NaN is NaN) ----
+            const uint32_t keep = mall ? 0xffffffffu : ((v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u));
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t r4[4];
+                const uint32_t a = vb + (q >> 1) * kSwHalf + rbase;
+                ldsm_x4_t(a + (((4u * (q & 1) + lm) ^ swz(a)) << 4), r4);
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    float(&a)[4] = acc[2 * q + hb];
+                    a[0] *= al0;
+                    a[1] *= al1;
+                    a[2] *= al0;
+                    a[3] *= al1;
+                    mma_k8<E>(a, r4[2 * hb] & keep, r4[2 * hb + 1] & keep, pb);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+            if (++stage == NS) {
+                stage = 0;
+                phase ^= 1;
+            }
+            if (!(mflags & kLast)) continue;
+
+            // ---- end of a segment: this warp's (max, sum, O) of each head into `red` ----
+            float l = l_part;
+            l += __shfl_xor_sync(kFull, l, 1);
+            l += __shfl_xor_sync(kFull, l, 2);
+            if (gq < G && tq == 0) {
+                float *rh = red + (cw * G + gq) * (D + 2);
+                rh[D] = m_run;
+                rh[D + 1] = l;
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int h = 2 * tq + hh;
+                if (h < G) {
+                    float *rh = red + (cw * G + h) * (D + 2);
+#pragma unroll
+                    for (int j = 0; j < KS; ++j) {
+                        rh[16 * j + gq] = acc[j][hh];
+                        rh[16 * j + gq + 8] = acc[j][2 + hh];
+                    }
+                }
+            }
+            if (!combine(mflags, mb, mg)) return;
+        }
+    } else {
+        const int r = lane % S::LPP;
+        const int rg = lane / S::LPR, cc = lane % S::LPR;
+        // softmax: lane handles row spos of heads shead + HPR * k (HPR = 32 / rows per warp)
+        const int spos = lane % kWPos, shead = lane / kWPos;
+        float *sb = sbuf + cw * G * kWPos;
+        float *pb = pbuf + cw * G * kWPos;
+        float *ab = abuf + cw * G;
+
+        uint64_t q2[G][S::CPL][4];
+        uint64_t acc[G][S::NPV];
+        float m_run[S::ROUNDS], l_part[S::ROUNDS];
+        int stage = 0;
+        uint32_t phase = 0;
+
+        for (long long i = 0; i < count; ++i) {
+            bool ok = warp_wait(full0 + 8 * stage, phase, abort_flag);
+            if (!ok) {
+                if (lane == 0) {
+                    raise_err(p.err, PA_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                return;
+            }
+            const TileMeta &m = metas[stage];
+            const int mflags = m.flags, mb = m.b, mg = m.g, mall = m.all_valid, mnew = m.newrow;
+            const unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
+            const uint32_t kb = smem_addr(st), vb = kb + S::TILE_BYTES;
+            // this warp's rows as a validity mask (bit rl: row rl of the warp)
+            const unsigned vrows = warp_rows_valid(m, cw);
+
+            if (mflags & kFirst) {
+                const T *qs = reinterpret_cast<const T *>(st + 2 * S::TILE_BYTES);
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int c = 0; c < S::CPL; ++c) {
+                        const int j = S::chunk(c, r, (lane / S::LPP));
+                        const uint4 u = *reinterpret_cast<const uint4 *>(qs + h * D + j * 8);
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = E::unpack2(w[e]);
+                            q2[h][c][e] = f2_pack(f.x * p.scale_log2, f.y * p.scale_log2);
+                        }
+                    }
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int e = 0; e < S::NPV; ++e) acc[h][e] = 0;
+#pragma unroll
+                for (int k = 0; k < S::ROUNDS; ++k) {
+                    m_run[k] = -INFINITY;
+                    l_part[k] = 0.f;
+                }
+            }
+
+            // ---- scores of this warp's 16 rows ----
+#pragma unroll
+            for (int pass = 0; pass < S::PASSES; ++pass) {
+                const int u = lane / S::LPP;
+                const int rl = pass * S::PPP + u;  // row within the warp's 16
+                const int row = cw * kWPos + rl;
+                uint64_t d2[G][S::CPL];
+#pragma unroll
+                for (int c = 0; c < S::CPL; ++c) {
+                    const uint4 kv = lds128(kb + (row == mnew ? kTN : row) * D * 2 + S::chunk(c, r, u) * 16);
+                    const uint64_t k0 = unpack_pair<E>(kv.x), k1 = unpack_pair<E>(kv.y);
+                    const uint64_t k2 = unpack_pair<E>(kv.z), k3 = unpack_pair<E>(kv.w);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        uint64_t a = f2_mul(q2[h][c][0], k0);
+                        a = f2_fma(q2[h][c][1], k1, a);
+                        a = f2_fma(q2[h][c][2], k2, a);
+                        d2[h][c] = f2_fma(q2[h][c][3], k3, a);
+                    }
+                }
+                float dot[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    // pairwise tree over the chunks keeps the dependency chain short
+                    uint64_t t2 = d2[h][0];
+#pragma unroll
+                    for (int c = 1; c < S::CPL; ++c) t2 = f2_add(t2, d2[h][c]);
+                    dot[h] = f2_lo(t2) + f2_hi(t2);
+                }
+#pragma unroll
+                for (int o = S::LPP / 2; o >= 1; o >>= 1)
+#pragma unroll
+                    for (int h = 0; h < G; ++h) dot[h] += __shfl_xor_sync(kFull, dot[h], o);
+                if (r == 0) {
+                    const bool valid = (vrows >> rl) & 1u;
+#pragma unroll
+                    for (int h = 0; h < G; ++h) sb[h * kWPos + rl] = valid ? dot[h] : -INFINITY;
+                }
+            }
+            __syncwarp();
+
+            // ---- online softmax over the 16 rows ----
+#pragma unroll
+            for (int k = 0; k < S::ROUNDS; ++k) {
+                const int h = shead + S::HPR * k;
+                const bool act = h < G;
+                const float s = act ? sb[h * kWPos + spos] : -INFINITY;
+                float mt = s;
+#pragma unroll
+                for (int o = kWPos / 2; o >= 1; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, o));
+                const float m_new = fmaxf(m_run[k], mt);
+                const float mu = m_new == -INFINITY ? 0.f : m_new;
+                const float alpha = fast_exp2(m_run[k] - mu);
+                m_run[k] = m_new;
+                const float pr = fast_exp2(s - mu);
+                l_part[k] = fmaf(l_part[k], alpha, pr);
+                if (act) {
+                    pb[h * kWPos + spos] = pr;
+                    if (spos == 0) ab[h] = alpha;
+                }
+            }
+            __syncwarp();
+
+            // ---- O = alpha O + P V ----
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float al = ab[h];
+                const uint64_t a2 = f2_pack(al, al);
+#pragma unroll
+                for (int e = 0; e < S::NPV; ++e) acc[h][e] = f2_mul(acc[h][e], a2);
+            }
+            auto pv_row = [&](int rl) {
+                const int row0 = cw * kWPos + rl;
+                const int row = row0 == mnew ? kTN : row0;
+                uint64_t v[S::NPV];
+                if constexpr (S::CPV == 8) {
+                    const uint4 vv = lds128(vb + row * D * 2 + cc * 16);
+                    v[0] = unpack_pair<E>(vv.x);
+                    v[1] = unpack_pair<E>(vv.y);
+                    v[2] = unpack_pair<E>(vv.z);
+                    v[3] = unpack_pair<E>(vv.w);
+                } else {
+                    const uint2 vv = lds64(vb + row * D * 2 + cc * 8);
+                    v[0] = unpack_pair<E>(vv.x);
+                    v[1] = unpack_pair<E>(vv.y);
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float pr = pb[h * kWPos + rl];
+                    const uint64_t p2 = f2_pack(pr, pr);
+#pragma unroll
+                    for (int e = 0; e < S::NPV; ++e) acc[h][e] = f2_fma(p2, v[e], acc[h][e]);
+                }
+            };
+            if (mall) {
+#pragma unroll
+                for (int it = 0; it < S::PV_IT; ++it) pv_row(it * S::RPI + rg);
+            } else {
+                // rows outside the context are skipped: their stage bytes may hold anything
+#pragma unroll
+                for (int it = 0; it < S::PV_IT; ++it) {
+                    const int rl = it * S::RPI + rg;
+                    if ((vrows >> rl) & 1u) pv_row(rl);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+            if (++stage == NS) {
+                stage = 0;
+                phase ^= 1;
+            }
+
+            if (!(mflags & kLast)) continue;
+
+            // ---- end of a segment: combine the 8 warps ----
+            float *ro = red + cw * G * (D + 2);
+#pragma unroll
+            for (int k = 0; k < S::ROUNDS; ++k) {
+                float l = l_part[k];
+#pragma unroll
+                for (int o = kWPos / 2; o >= 1; o >>= 1) l += __shfl_xor_sync(kFull, l, o);
+                const int h = shead + S::HPR * k;
+                if (h < G && spos == 0) {
+                    ro[h * (D + 2) + D] = m_run[k];
+                    ro[h * (D + 2) + D + 1] = l;
+                }
+            }
+#pragma unroll
+            for (int o = S::LPR; o < 32; o <<= 1)
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int e = 0; e < S::NPV; ++e) {
+                        const float lo_ = f2_lo(acc[h][e]) + __shfl_xor_sync(kFull, f2_lo(acc[h][e]), o);
+                        const float hi_ = f2_hi(acc[h][e]) + __shfl_xor_sync(kFull, f2_hi(acc[h][e]), o);
+                        acc[h][e] = f2_pack(lo_, hi_);
+                    }
+            if (rg == 0)
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float *dst = ro + h * (D + 2) + cc * S::CPV;
+#pragma unroll
+                    for (int e = 0; e < S::NPV; ++e) {
+                        dst[2 * e] = f2_lo(acc[h][e]);
+                        dst[2 * e + 1] = f2_hi(acc[h][e]);
+                    }
+                }
+            if (!combine(mflags, mb, mg)) return;
+        }
     }
 }
 
@@ -790,26 +1059,33 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// swizzled: boxes of 64 columns with the 128-byte swizzle (tensor-core consumers); else whole
+// unswizzled rows
 bool encode_pool(CUtensorMap *m, const void *pool, pa_dtype dt, int D, int Hkv, long long slots,
-                 int box_rows) {
+                 int box_rows, bool swizzled) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
                           static_cast<cuuint64_t>(slots > 0 ? slots : 1)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hkv) * D * 2};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(swizzled ? 64 : D), 1, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
               const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D, int G>
 constexpr int stages_for() {
-    const int budget = kSmemPerSm / ctas_per_sm<G>() - 1024;
-    const int s = (budget - fixed_smem<D, G>()) / Shape<D, G>::STAGE_BYTES;
-    return s < 6 ? s : 6;
+    const int budget = kSmemPerSm / ctas_per_sm(D, G) - 1024;
+    // A multiple of the producer count, so that each stage belongs to one producer. (A stage that
+    // alternated between producers could not be waited on by parity: a producer cannot tell
+    // whether the other has armed the stage's previous phase yet, and a barrier two phases behind
+    // has the parity of the phase it waits for.)
+    const int s = (budget - fixed_smem<D, G>()) / Shape<D, G>::STAGE_BYTES / producers_for(G) * producers_for(G);
+    return s < kMaxStages ? s : kMaxStages;
 }
 
 template <int D, int G, class E>
@@ -827,9 +1103,9 @@ cudaError_t launch_typed(DecodeParams &prm, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev] = smem;
     }
-    const int P = device_sm_count() * ctas_per_sm<G>();
+    const int P = device_sm_count() * ctas_per_sm(D, G);
     if (P > kMergeMaxCtas) return cudaErrorInvalidConfiguration;
-    kern<<<P, kThreads, smem, stream>>>(prm);
+    kern<<<P, threads_for(G), smem, stream>>>(prm);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     decode_merge_kernel<D, G, E><<<P, 128, 0, stream>>>(prm);
@@ -859,7 +1135,7 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, in
     (void)block_size;
     DecodePlan plan{};
     const int G = Hq / Hkv;
-    const size_t P = static_cast<size_t>(device_sm_count()) * (G <= 3 ? 2 : 1);
+    const size_t P = static_cast<size_t>(device_sm_count()) * ctas_per_sm(D, G);
     const size_t part = P * 2 * G * (D + 2) * sizeof(float);
     plan.ws_bytes = (part + 255) / 256 * 256 + P * sizeof(SegRecord);
     return plan;
@@ -872,8 +1148,10 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     int R = 1;
     while (R < kTN && a.block_size % (2 * R) == 0) R *= 2;
     const long long slots = static_cast<long long>(a.num_blocks) * a.block_size;
-    if (!encode_pool(&prm.tmap_k, a.k_cache, a.dtype, a.D, a.Hkv, slots, R) ||
-        !encode_pool(&prm.tmap_v, a.v_cache, a.dtype, a.D, a.Hkv, slots, R))
+    const int G = a.Hq / a.Hkv;
+    const bool sw = G >= kMmaMinGroup;  // tensor-core consumers read swizzled tiles
+    if (!encode_pool(&prm.tmap_k, a.k_cache, a.dtype, a.D, a.Hkv, slots, R, sw) ||
+        !encode_pool(&prm.tmap_v, a.v_cache, a.dtype, a.D, a.Hkv, slots, R, sw))
         return cudaErrorInvalidValue;
     prm.q = a.q;
     prm.k_new = a.k_new;
@@ -883,8 +1161,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     prm.block_tables = a.block_tables;
     prm.context_lens = a.context_lens;
     prm.out = a.out;
-    const int G = a.Hq / a.Hkv;
-    const size_t P = static_cast<size_t>(device_sm_count()) * (G <= 3 ? 2 : 1);
+    const size_t P = static_cast<size_t>(device_sm_count()) * ctas_per_sm(a.D, G);
     const size_t part = P * 2 * G * (a.D + 2) * sizeof(float);
     prm.part = static_cast<float *>(a.workspace);
     prm.rec = reinterpret_cast<SegRecord *>(static_cast<char *>(a.workspace) + (part + 255) / 256 * 256);

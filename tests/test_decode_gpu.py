@@ -61,17 +61,21 @@ def test_group_sizes(orc, G, D, dt):
     _check_full(orc, c)
 
 
+# small groups (fp32 pipes, unswizzled tiles) and large groups (tensor-core fragments, swizzled
+# 64-column halves): the block size sets the TMA box height, 1 row up to 64
+@pytest.mark.parametrize("Hq,Hkv,D,dt", [(8, 4, 128, "bf16"), (14, 2, 64, "f16"), (16, 2, 128, "bf16")])
 @pytest.mark.parametrize("bs", [1, 3, 4, 16, 64, 256])
-def test_block_sizes(orc, bs):
+def test_block_sizes(orc, bs, Hq, Hkv, D, dt):
     lens = [1, 2, bs, bs + 1, 129, 511, 1000]
-    c = W.decode_case(B=len(lens), Hq=8, Hkv=4, D=128, block_size=bs, dtype="bf16",
+    c = W.decode_case(B=len(lens), Hq=Hq, Hkv=Hkv, D=D, block_size=bs, dtype=dt,
                       context_lens=lens, seed=bs, placement="interleaved")
     _check_full(orc, c)
 
 
-def test_zero_context_and_padding_rows(orc):
+@pytest.mark.parametrize("Hq", [4, 14])
+def test_zero_context_and_padding_rows(orc, Hq):
     lens = [0, 5, 0, 300]
-    c = W.decode_case(B=4, Hq=4, Hkv=2, D=64, block_size=16, dtype="f16", context_lens=lens,
+    c = W.decode_case(B=4, Hq=Hq, Hkv=2, D=64, block_size=16, dtype="f16", context_lens=lens,
                       seed=3, pad_slots=0)
     run = DecodeRun(c)
     out = f64(run.step())
@@ -80,13 +84,15 @@ def test_zero_context_and_padding_rows(orc):
     assert max_abs(out, _reference(orc, c, kc_ref, vc_ref)) <= TOL["f16"]
 
 
-def test_single_token_returns_its_value(orc):
-    c = W.decode_case(B=3, Hq=6, Hkv=3, D=128, block_size=256, dtype="bf16", context_lens=[1, 1, 1],
-                      seed=4)
+@pytest.mark.parametrize("Hq,Hkv", [(6, 3), (24, 3)])
+def test_single_token_returns_its_value(orc, Hq, Hkv):
+    c = W.decode_case(B=3, Hq=Hq, Hkv=Hkv, D=128, block_size=256, dtype="bf16",
+                      context_lens=[1, 1, 1], seed=4)
     out = f64(DecodeRun(c).step())
     v = (c.v_new.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    for h in range(6):
-        assert np.array_equal(out[:, h], v[:, h // 2])
+    G = Hq // Hkv
+    for h in range(Hq):
+        assert np.array_equal(out[:, h], v[:, h // G])
 
 
 def test_max_context(orc):
@@ -110,8 +116,9 @@ def test_batch_equals_alone():
         assert max_abs(f64(out[0]), f64(batched[i])) <= TOL[c.dtype]
 
 
-def test_invalid_table_entry_is_flagged_and_masked(orc):
-    c = W.decode_case(B=2, Hq=4, Hkv=2, D=64, block_size=16, dtype="f16", context_lens=[40, 40],
+@pytest.mark.parametrize("Hq", [4, 14])
+def test_invalid_table_entry_is_flagged_and_masked(orc, Hq):
+    c = W.decode_case(B=2, Hq=Hq, Hkv=2, D=64, block_size=16, dtype="f16", context_lens=[40, 40],
                       seed=6)
     bt = c.block_tables.copy()
     bt[1, 1] = c.num_blocks + 7          # positions 16..31 of sequence 1 point outside the pool
@@ -155,8 +162,8 @@ def test_empty_batch_is_noop():
     torch.cuda.synchronize()
 
 
-def _sampled_full_size(orc, name, nsample=12):
-    c = W.make(name)
+def _sampled_full_size(orc, name, nsample=12, case=None):
+    c = W.make(name) if case is None else case
     run = DecodeRun(c)
     out = f64(run.step())
     assert int(run.err.item()) == 0
@@ -175,3 +182,17 @@ def _sampled_full_size(orc, name, nsample=12):
 @pytest.mark.parametrize("name", ["qwen25_05b_decode", "qwen3_06b_decode", "longtail_decode"])
 def test_full_size_sampled(orc, name):
     _sampled_full_size(orc, name)
+
+
+@pytest.mark.parametrize("G,Hkv,D,bs,dt", [(7, 2, 64, 16, "f16"), (8, 2, 128, 256, "bf16"),
+                                           (4, 4, 128, 16, "bf16"), (2, 8, 128, 256, "bf16")])
+def test_many_tiles_per_cta_sampled(orc, G, Hkv, D, bs, dt):
+    """About a hundred tiles per CTA: the stage ring wraps many times, so every stage passes
+    through many barrier phases and, with two producers, each producer's stages alternate with
+    the other's. Sampled sequences against the oracle; the error word (which a timed-out wait
+    would set) stays clear."""
+    rng = np.random.default_rng(11)
+    lens = rng.integers(100, 4096, size=256, endpoint=True)
+    c = W.decode_case(B=256, Hq=G * Hkv, Hkv=Hkv, D=D, block_size=bs, dtype=dt, context_lens=lens,
+                      seed=12)
+    _sampled_full_size(orc, None, nsample=8, case=c)
