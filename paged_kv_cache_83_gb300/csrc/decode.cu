@@ -262,6 +262,9 @@ __global__ void __launch_bounds__(threads_for(G), ctas_per_sm(D, G)) decode_kern
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = gridDim.x, cta = blockIdx.x;
     const long long cap = static_cast<long long>(p.max_blocks) * p.geom.block_size;
+    // the merge kernel may be launched now: it waits for this grid's completion before it reads
+    // anything, so only its launch overlaps this grid
+    asm volatile("griddepcontrol.launch_dependents;");
     const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + NS),
                    cons0 = smem_addr(bars + 2 * NS);
 
@@ -979,6 +982,9 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant
     __shared__ float norm[G];
     __shared__ int nseg_s;
     const int c = blockIdx.x, P = gridDim.x, tid = threadIdx.x, lane = tid & 31;
+    // launched ahead of time (programmatic dependent launch): wait until the decode grid has
+    // completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const SegRecord rc = p.rec[c];
     if (rc.b < 0 || rc.pair_start >= rc.lo || rc.pair_start + rc.ntiles > rc.hi) return;
     // first CTA whose range holds the pair's first tile: max{c' : lo(c') <= pair_start}
@@ -1108,8 +1114,19 @@ cudaError_t launch_typed(DecodeParams &prm, cudaStream_t stream) {
     kern<<<P, threads_for(G), smem, stream>>>(prm);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    decode_merge_kernel<D, G, E><<<P, 128, 0, stream>>>(prm);
-    return cudaGetLastError();
+    // the merge kernel as a programmatic dependent of the decode kernel: its launch overlaps the
+    // decode grid's tail instead of following it
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(P);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, G, E>, prm);
 }
 
 template <int D, class E>
