@@ -54,8 +54,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # profiles/decode_kernel_qwen3_06b_decode.md and profiles/prefill_tc_kernel_prefill_prefix.md
 # (layer 0 of the default workload; prefill_prefix). Each is valid only for the kernel sources it
 # was taken on, identified by their hash; after any change the bench reports null.
-DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_281_701_888,
-                  "sha256": "4d0d0fd0766a3cc4dbe61ee7d8d57f4f09a7a511e0a740b165867b6afa7ca5e8"}
+DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_281_796_352,
+                  "sha256": "844a4d0c467a07b17dcb6bea04faeaea1e337e56c90e1105701cc0c0f169c30b"}
 PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 411_089_920,
                    "sha256": "d56841fd65495c1c9a79fd3c92669449ba16f74585a2c9c6b73af500664f8661"}
 
@@ -410,6 +410,8 @@ def run_gpu(args, ws_, rank, local):
         rows.update(bench_prefill(torch, pa, dev, stream, bf16_peak, hbm, args))
     if not args.skip_small:
         rows["decode_small_graphs"] = bench_small_decode(torch, pa, dev, hbm)
+    if not args.skip_groups:
+        rows["decode_group_sweep"] = bench_group_sweep(torch, pa, dev, hbm)
     if rank == 0 and not args.skip_cpu:
         rows["block_manager"] = bench_block_manager(pa)
     st_mean = statistics.mean(st_ms)
@@ -526,6 +528,44 @@ def bench_small_decode(torch, pa, dev, hbm) -> dict:
     return res
 
 
+# GQA group sizes of common model shapes beyond the two named decode workloads: 256 sequences,
+# contexts U[100, 4096] (seeded), each KV set larger than L2
+GROUP_SWEEP = ((4, 4, 128, 256, "bf16"), (7, 2, 64, 16, "f16"), (8, 2, 128, 256, "bf16"))
+
+
+def bench_group_sweep(torch, pa, dev, hbm) -> dict:
+    """pa_decode across GQA group sizes G = Hq / Hkv (G >= 4 runs the tensor-core consumers),
+    timed with an L2 flush between iterations."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    res = {}
+    for G, Hkv, D, bs, dt in GROUP_SWEEP:
+        lens = np.random.default_rng(0).integers(100, 4096, size=256, endpoint=True)
+        c = W.decode_case(B=256, Hq=G * Hkv, Hkv=Hkv, D=D, block_size=bs, dtype=dt,
+                          context_lens=lens, seed=1)
+        L = DecodeLayer(torch, pa, c, dev)
+        run = lambda: pa.pa_decode(L.out, L.q, L.kc, L.vc, L.bt, L.cl, c.scale, workspace=L.ws)
+        for _ in range(3):
+            run()
+        ts = []
+        for _ in range(20):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            run()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        kv = kv_bytes(c.context_lens, c.Hkv, c.D)
+        res[f"G{G}_Hkv{Hkv}_D{D}_bs{bs}_{dt}"] = {
+            "us": ms * 1e3, "kv_bytes": kv, "GB_per_s": kv / (ms * 1e-3) / 1e9,
+            "frac_of_hbm": kv / (ms * 1e-3) / 1e9 / hbm,
+            "consumers": "tensor-core fragments" if G >= 4 else "fp32"}
+        del L
+        torch.cuda.empty_cache()
+    return res
+
+
 def bench_block_manager(pa) -> dict:
     """The host block manager on a serving-shaped trace: 256 sequences that share a 512-token
     system prompt, 256-token blocks; admit all, 256 decode appends each, release all. Timed
@@ -616,6 +656,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-small", action="store_true",
                     help="skip the CUDA-graph timing of the two small decode workloads")
+    ap.add_argument("--skip-groups", action="store_true",
+                    help="skip the decode timing across GQA group sizes")
     ap.add_argument("--layers", type=int, default=2, help="layers whose pools alternate")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clock-tail", action="store_true")
