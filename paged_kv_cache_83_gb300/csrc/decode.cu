@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(threads_for(G), ctas_per_sm(D, G)) decode_kern
     const int P = gridDim.x, cta = blockIdx.x;
     const long long cap = static_cast<long long>(p.max_blocks) * p.geom.block_size;
     // the merge kernel may be launched now: it waits for this grid's completion before it reads
-    // anything, so only its launch overlaps this grid
+    // anything, so only its launch overlaps this grid (it is also why the wait below comes after
+    // the shared-memory setup: that part overlaps the grid before this one)
     asm volatile("griddepcontrol.launch_dependents;");
     const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + NS),
                    cons0 = smem_addr(bars + 2 * NS);
@@ -279,54 +280,87 @@ __global__ void __launch_bounds__(threads_for(G), ctas_per_sm(D, G)) decode_kern
         fence_mbar_init();
     }
 
-    // ---- pass 1: tiles per sequence, the total, zero rows of empty sequences ----
-    long long mine = 0;
-    for (int b = tid; b < p.B; b += kThreads) {
-        const int n = p.context_lens[b];
-        if (n < 0 || n > cap) {
-            if (b % P == cta) raise_err(p.err, PA_DEVERR_LENGTH);
-        }
-        const int nt = ntiles_of(p, b, cap);
-        mine += nt;
+    // launched as a programmatic dependent: nothing this grid reads may be touched before the
+    // grids it depends on have completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // zero rows of a sequence without positions (and flag lengths outside the table)
+    auto check_seq = [&](int b, int n) -> int {
+        if ((n < 0 || n > cap) && b % P == cta) raise_err(p.err, PA_DEVERR_LENGTH);
+        const int nt = (n <= 0 || n > cap) ? 0 : (n + kTN - 1) / kTN;
         if (nt == 0 && b % P == cta) {
             uint4 *o = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + static_cast<size_t>(b) * p.Hq * D);
             for (int i = 0; i < p.Hq * D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
         }
-    }
-    const long long total = block_sum<kThreads>(mine, scan) * p.Hkv;
-    const long long lo = total * cta / P, hi = total * (cta + 1) / P;
-
-    // ---- pass 2: the (b, g, t) of tile `lo` ----
-    if (tid == 0) scan[16] = -1;
-    __syncthreads();
-    if (lo < hi) {
-        long long running = 0;  // tiles of sequences before this chunk, times Hkv
-        for (int base = 0; base < p.B; base += kThreads) {
-            const int b = base + tid;
-            const int nt = b < p.B ? ntiles_of(p, b, cap) : 0;
-            long long v = nt;  // inclusive scan of nt across the block
-            for (int o = 1; o < 32; o <<= 1) {
-                const long long x = __shfl_up_sync(kFull, v, o);
-                if (lane >= o) v += x;
-            }
-            if (lane == 31) scan[warp] = v;
-            __syncthreads();
-            long long before = 0, chunk_total = 0;
-            for (int i = 0; i < kThreads / 32; ++i) {
-                if (i < warp) before += scan[i];
-                chunk_total += scan[i];
-            }
-            const long long excl = running + (before + v - nt) * p.Hkv;
-            if (nt > 0 && excl <= lo && lo < excl + static_cast<long long>(nt) * p.Hkv) {
-                scan[16] = b;
-                scan[17] = excl;
-            }
-            running += chunk_total * p.Hkv;
-            __syncthreads();
-            if (running > lo) break;  // uniform: every thread sees the same `running`
+        return nt;
+    };
+    long long total, lo, hi;
+    if (p.B <= kThreads) {
+        // ---- one pass: each thread one sequence; a block scan of the tile counts gives the
+        // total and the (b, g, t) of tile `lo` ----
+        const int nt = tid < p.B ? check_seq(tid, p.context_lens[tid]) : 0;
+        long long v = nt;  // inclusive scan of nt across the block
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long x = __shfl_up_sync(kFull, v, o);
+            if (lane >= o) v += x;
         }
+        if (lane == 31) scan[warp] = v;
+        if (tid == 0) scan[16] = -1;
+        __syncthreads();
+        long long before = 0, all = 0;
+        for (int i = 0; i < kThreads / 32; ++i) {
+            if (i < warp) before += scan[i];
+            all += scan[i];
+        }
+        total = all * p.Hkv;
+        lo = total * cta / P;
+        hi = total * (cta + 1) / P;
+        const long long excl = (before + v - nt) * p.Hkv;
+        if (lo < hi && nt > 0 && excl <= lo && lo < excl + static_cast<long long>(nt) * p.Hkv) {
+            scan[16] = tid;
+            scan[17] = excl;
+        }
+        __syncthreads();
+    } else {
+        // ---- pass 1: tiles per sequence, the total ----
+        long long mine = 0;
+        for (int b = tid; b < p.B; b += kThreads) mine += check_seq(b, p.context_lens[b]);
+        total = block_sum<kThreads>(mine, scan) * p.Hkv;
+        lo = total * cta / P;
+        hi = total * (cta + 1) / P;
+
+        // ---- pass 2: the (b, g, t) of tile `lo` ----
+        if (tid == 0) scan[16] = -1;
+        __syncthreads();
+        if (lo < hi) {
+            long long running = 0;  // tiles of sequences before this chunk, times Hkv
+            for (int base = 0; base < p.B; base += kThreads) {
+                const int b = base + tid;
+                const int nt = b < p.B ? ntiles_of(p, b, cap) : 0;
+                long long v = nt;  // inclusive scan of nt across the block
+                for (int o = 1; o < 32; o <<= 1) {
+                    const long long x = __shfl_up_sync(kFull, v, o);
+                    if (lane >= o) v += x;
+                }
+                if (lane == 31) scan[warp] = v;
+                __syncthreads();
+                long long before = 0, chunk_total = 0;
+                for (int i = 0; i < kThreads / 32; ++i) {
+                    if (i < warp) before += scan[i];
+                    chunk_total += scan[i];
+                }
+                const long long excl = running + (before + v - nt) * p.Hkv;
+                if (nt > 0 && excl <= lo && lo < excl + static_cast<long long>(nt) * p.Hkv) {
+                    scan[16] = b;
+                    scan[17] = excl;
+                }
+                running += chunk_total * p.Hkv;
+                __syncthreads();
+                if (running > lo) break;  // uniform: every thread sees the same `running`
+            }
+        }
+        __syncthreads();
     }
-    __syncthreads();
     const int b0 = static_cast<int>(scan[16]);
     const long long seq_start = scan[17];  // global index of tile (b0, 0, 0)
 
@@ -982,6 +1016,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant
     __shared__ float norm[G];
     __shared__ int nseg_s;
     const int c = blockIdx.x, P = gridDim.x, tid = threadIdx.x, lane = tid & 31;
+    // what follows in the stream may launch now (it waits for this grid before reading)
+    asm volatile("griddepcontrol.launch_dependents;");
     // launched ahead of time (programmatic dependent launch): wait until the decode grid has
     // completed and its writes are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1111,19 +1147,26 @@ cudaError_t launch_typed(DecodeParams &prm, cudaStream_t stream) {
     }
     const int P = device_sm_count() * ctas_per_sm(D, G);
     if (P > kMergeMaxCtas) return cudaErrorInvalidConfiguration;
-    kern<<<P, threads_for(G), smem, stream>>>(prm);
-    cudaError_t e = cudaGetLastError();
+    // both kernels launch as programmatic dependents of what precedes them in the stream: a
+    // launch overlaps the tail of the grid before it, and each kernel waits on the grid
+    // dependency before it reads anything
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t dcfg{};
+    dcfg.gridDim = dim3(P);
+    dcfg.blockDim = dim3(threads_for(G));
+    dcfg.dynamicSmemBytes = smem;
+    dcfg.stream = stream;
+    dcfg.attrs = attr;
+    dcfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&dcfg, kern, prm);
     if (e != cudaSuccess) return e;
-    // the merge kernel as a programmatic dependent of the decode kernel: its launch overlaps the
-    // decode grid's tail instead of following it
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(P);
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, G, E>, prm);
