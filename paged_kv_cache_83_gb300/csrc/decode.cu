@@ -69,8 +69,8 @@ constexpr bool use_mma() { return G >= kMmaMinGroup; }
 __host__ __device__ constexpr int ctas_per_sm(int D, int G) { return G < kMmaMinGroup ? 2 : 1; }
 // producer warps (alternate tiles): two keep the light tensor-core consumers fed; with the fp32
 // consumers one suffices and a second only takes issue slots from them
-__host__ __device__ constexpr int producers_for(int G) { return G < kMmaMinGroup ? 1 : 2; }
-__host__ __device__ constexpr int threads_for(int G) { return 32 * (producers_for(G) + kConsumers); }
+__host__ __device__ constexpr int producers_for(int D, int G) { return G < kMmaMinGroup ? 1 : 2; }
+__host__ __device__ constexpr int threads_for(int D, int G) { return 32 * (producers_for(D, G) + kConsumers); }
 // one swizzled tile half: 64 rows + the spare row of 128 bytes. The 128-byte swizzle is a
 // function of the shared-memory address (16-byte chunk c of the 128-byte line at address a sits
 // at c ^ ((a >> 7) & 7)), so halves need only 128-byte alignment and readers take the phase from
@@ -158,7 +158,7 @@ template <int D, int G>
 constexpr int fixed_smem() {
     // + metas, barriers, scan scratch (1 KB), the slack that aligns the ring (1 KB) and the
     // producer's ring of prepared tiles
-    return Shape<D, G>::RED_BYTES + Shape<D, G>::SCRATCH_BYTES + 2048 + producers_for(G) * kIdRing * (kTN * 4 + 32);
+    return Shape<D, G>::RED_BYTES + Shape<D, G>::SCRATCH_BYTES + 2048 + producers_for(D, G) * kIdRing * (kTN * 4 + 32);
 }
 
 // All 32 lanes wait for the phase, then the warp reconverges; false (for every lane) if the wait
@@ -239,9 +239,9 @@ __device__ long long block_sum(long long v, long long *red) {
 }
 
 template <int D, int G, class E>
-__global__ void __launch_bounds__(threads_for(G), ctas_per_sm(D, G)) decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_kernel(const __grid_constant__ DecodeParams p) {
     using S = Shape<D, G>;
-    constexpr int kProducers = producers_for(G), kThreads = threads_for(G);
+    constexpr int kProducers = producers_for(D, G), kThreads = threads_for(D, G);
     using T = typename E::T;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // stages start on a 1024-byte boundary (the launch adds 1 KB of slack for this)
@@ -1115,7 +1115,10 @@ bool encode_pool(CUtensorMap *m, const void *pool, pa_dtype dt, int D, int Hkv, 
     return fn(m, dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
               const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              // L2 fills no wider than one head's row: a 256-byte fill of a 128-byte row (D = 64)
+              // also pulls in the next head's row, which another tile reads much later (measured:
+              // 1.44x the KV bytes from DRAM)
+              D * 2 >= 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1126,8 +1129,9 @@ constexpr int stages_for() {
     // alternated between producers could not be waited on by parity: a producer cannot tell
     // whether the other has armed the stage's previous phase yet, and a barrier two phases behind
     // has the parity of the phase it waits for.)
-    const int s = (budget - fixed_smem<D, G>()) / Shape<D, G>::STAGE_BYTES / producers_for(G) * producers_for(G);
-    return s < kMaxStages ? s : kMaxStages;
+    constexpr int np = producers_for(D, G);
+    const int s = (budget - fixed_smem<D, G>()) / Shape<D, G>::STAGE_BYTES / np * np;
+    return s < kMaxStages / np * np ? s : kMaxStages / np * np;
 }
 
 template <int D, int G, class E>
@@ -1155,7 +1159,7 @@ cudaError_t launch_typed(DecodeParams &prm, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t dcfg{};
     dcfg.gridDim = dim3(P);
-    dcfg.blockDim = dim3(threads_for(G));
+    dcfg.blockDim = dim3(threads_for(D, G));
     dcfg.dynamicSmemBytes = smem;
     dcfg.stream = stream;
     dcfg.attrs = attr;
