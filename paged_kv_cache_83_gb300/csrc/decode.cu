@@ -45,14 +45,13 @@ namespace pa {
 
 namespace {
 
-constexpr int kTN = 64;                  // positions per tile
+constexpr int kTN = 64;                  // positions per consumer tile (a stage holds 1 or 2)
 constexpr int kConsumers = 8;            // consumer warps
 constexpr int kWPos = kTN / kConsumers;  // rows per consumer warp per tile
 constexpr int kConsThreads = 32 * kConsumers;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kSmemPerSm = 227 * 1024;
 constexpr int kMaxStages = 8;  // the tile metas and barriers of 8 stages fit their 1 KB
-constexpr int kLaneBoxes = (kTN + 31) / 32;  // TMA boxes per producer lane and tile, at most
 constexpr int kLook = 2;                     // a producer's steps prepared ahead of the one it issues
 constexpr int kIdRing = 4;                   // each producer's ring of prepared tiles (> kLook)
 static_assert(kIdRing > kLook && (kIdRing & (kIdRing - 1)) == 0, "block-id ring");
@@ -71,12 +70,6 @@ __host__ __device__ constexpr int ctas_per_sm(int D, int G) { return G < kMmaMin
 // consumers one suffices and a second only takes issue slots from them
 __host__ __device__ constexpr int producers_for(int D, int G) { return G < kMmaMinGroup ? 1 : 2; }
 __host__ __device__ constexpr int threads_for(int D, int G) { return 32 * (producers_for(D, G) + kConsumers); }
-// one swizzled tile half: 64 rows + the spare row of 128 bytes. The 128-byte swizzle is a
-// function of the shared-memory address (16-byte chunk c of the 128-byte line at address a sits
-// at c ^ ((a >> 7) & 7)), so halves need only 128-byte alignment and readers take the phase from
-// the address.
-constexpr int kSwRows = kTN + 1;
-constexpr int kSwHalf = kSwRows * 128;
 
 // flags of one tile
 constexpr int kFirst = 1;  // first tile of a segment: reset the state, read q
@@ -133,10 +126,20 @@ struct Shape {
     static constexpr int HPR = 32 / kWPos;                    // softmax heads per round
     static constexpr int ROUNDS = (G + HPR - 1) / HPR;
     static constexpr bool MMA = use_mma<G>();
+    // positions per stage: 128 for the tensor-core path at D = 64 (as many bytes per stage, and as
+    // much producer work per byte, as at D = 128), else 64; consumers take it 64 rows at a time
+    static constexpr int TN = (MMA && D == 64) ? 2 * kTN : kTN;
+    static constexpr int SUB = TN / kTN;
+    static constexpr int LANE_BOXES = TN / 32;  // TMA boxes per producer lane and stage, at most
     static constexpr int NH = D / 64;  // 64-column halves of a swizzled tile
+    // one swizzled tile half: TN rows + the spare row, 128 bytes each. The 128-byte swizzle is a
+    // function of the shared-memory address (16-byte chunk c of the 128-byte line at address a
+    // sits at c ^ ((a >> 7) & 7)), so halves need only 128-byte alignment and readers take the
+    // phase from the address.
+    static constexpr int SW_HALF = (TN + 1) * 128;
     // 64 rows + a spare row that takes a new token's K (or V) row in the fused store + decode;
     // tensor-core consumers: NH swizzled halves of 128-byte rows
-    static constexpr int TILE_BYTES = MMA ? NH * kSwHalf : (kTN + 1) * D * 2;
+    static constexpr int TILE_BYTES = MMA ? NH * SW_HALF : (TN + 1) * D * 2;
     static constexpr int Q_BYTES = G * D * 2;
     // stages on 1 KB boundaries for the unswizzled tiles; 128 bytes suffice for the swizzled ones
     static constexpr int STAGE_ALIGN = MMA ? 128 : 1024;
@@ -158,7 +161,7 @@ template <int D, int G>
 constexpr int fixed_smem() {
     // + metas, barriers, scan scratch (1 KB), the slack that aligns the ring (1 KB) and the
     // producer's ring of prepared tiles
-    return Shape<D, G>::RED_BYTES + Shape<D, G>::SCRATCH_BYTES + 2048 + producers_for(D, G) * kIdRing * (kTN * 4 + 32);
+    return Shape<D, G>::RED_BYTES + Shape<D, G>::SCRATCH_BYTES + 2048 + producers_for(D, G) * kIdRing * (Shape<D, G>::TN * 4 + 32);
 }
 
 // All 32 lanes wait for the phase, then the warp reconverges; false (for every lane) if the wait
@@ -170,9 +173,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return all;
 }
 
-// validity of consumer warp cw's kWPos rows, as the low bits of a word
-__device__ __forceinline__ unsigned warp_rows_valid(const TileMeta &m, int cw) {
-    const int first = cw * kWPos;
+// validity of the kWPos rows of consumer warp cw in 64-row sub-tile `sub`, as the low bits of a word
+__device__ __forceinline__ unsigned warp_rows_valid(const TileMeta &m, int cw, int sub = 0) {
+    const int first = sub * kTN + cw * kWPos;
     const unsigned long long w = m.valid[first >> 6];
     return static_cast<unsigned>(w >> (first & 63)) & ((1u << kWPos) - 1u);
 }
@@ -219,10 +222,12 @@ __device__ __forceinline__ void mma_k8(float (&d)[4], uint32_t a0, uint32_t a1, 
             : "r"(a0), "r"(a1), "r"(b0));
 }
 
+// stages of TN positions over sequence b's context
+template <int TN>
 __device__ __forceinline__ int ntiles_of(const DecodeParams &p, int b, long long cap) {
     const int n = p.context_lens[b];
     if (n <= 0 || n > cap) return 0;
-    return (n + kTN - 1) / kTN;
+    return (n + TN - 1) / TN;
 }
 
 // block-wide sum over all NT threads; `red` holds NT / 32 longs
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
     long long *scan = reinterpret_cast<long long *>(bars + 2 * NS + 2);  // 16 longs + start
     volatile int *abort_flag = reinterpret_cast<volatile int *>(scan + 20);
     PrepTile *prep = reinterpret_cast<PrepTile *>(scan + 24);  // [producers][kIdRing]
-    int *idring = reinterpret_cast<int *>(prep + kProducers * kIdRing);  // [producers][kIdRing][kTN]
+    int *idring = reinterpret_cast<int *>(prep + kProducers * kIdRing);  // [producers][kIdRing][TN]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = gridDim.x, cta = blockIdx.x;
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
     // zero rows of a sequence without positions (and flag lengths outside the table)
     auto check_seq = [&](int b, int n) -> int {
         if ((n < 0 || n > cap) && b % P == cta) raise_err(p.err, PA_DEVERR_LENGTH);
-        const int nt = (n <= 0 || n > cap) ? 0 : (n + kTN - 1) / kTN;
+        const int nt = (n <= 0 || n > cap) ? 0 : (n + S::TN - 1) / S::TN;
         if (nt == 0 && b % P == cta) {
             uint4 *o = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + static_cast<size_t>(b) * p.Hq * D);
             for (int i = 0; i < p.Hq * D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
             long long running = 0;  // tiles of sequences before this chunk, times Hkv
             for (int base = 0; base < p.B; base += kThreads) {
                 const int b = base + tid;
-                const int nt = b < p.B ? ntiles_of(p, b, cap) : 0;
+                const int nt = b < p.B ? ntiles_of<S::TN>(p, b, cap) : 0;
                 long long v = nt;  // inclusive scan of nt across the block
                 for (int o = 1; o < 32; o <<= 1) {
                     const long long x = __shfl_up_sync(kFull, v, o);
@@ -371,7 +376,7 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
         r.total = total;
         r.b = -1;
         if (lo < hi && b0 >= 0) {
-            const int nt = ntiles_of(p, b0, cap);
+            const int nt = ntiles_of<S::TN>(p, b0, cap);
             const long long off = lo - seq_start;
             r.b = b0;
             r.g = static_cast<int>(off / nt);
@@ -392,12 +397,13 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
             prefetch_tmap(&p.tmap_k);
             prefetch_tmap(&p.tmap_v);
         }
-        const int R = p.box_rows, nbox = kTN / R;
+        constexpr int TN = S::TN;
+        const int R = p.box_rows, nbox = TN / R;
         const uint32_t box_bytes = static_cast<uint32_t>(R) * D * 2;
         const unsigned long long box_rows_mask = R == 64 ? ~0ull : ((1ull << R) - 1ull);
         // walker: the next tile to prepare
         int b = b0;
-        int nt = ntiles_of(p, b, cap);
+        int nt = ntiles_of<S::TN>(p, b, cap);
         int n = p.context_lens[b];
         const long long off = lo - seq_start;
         int g = static_cast<int>(off / nt), t = static_cast<int>(off % nt);
@@ -411,14 +417,14 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
                     g = 0;
                     do {
                         ++b;
-                    } while (b < p.B && (nt = ntiles_of(p, b, cap)) == 0);
+                    } while (b < p.B && (nt = ntiles_of<S::TN>(p, b, cap)) == 0);
                     if (b < p.B) n = p.context_lens[b];
                 }
             }
         };
         for (int k = 0; k < pw && k < count; ++k) advance();
         PrepTile *myprep = prep + pw * kIdRing;
-        int *myids = idring + pw * kIdRing * kTN;
+        int *myids = idring + pw * kIdRing * TN;
         // Each producer prepares its tiles kLook of its own steps ahead of the one it issues:
         // preparing records the tile's coordinates and queues cp.async copies of its block ids
         // (lane l: boxes l and l + 32) into a ring in shared memory, so the block-table reads are
@@ -426,13 +432,13 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
         auto prepare = [&](long long j) {
             const int sl = static_cast<int>(j % kIdRing);
             if (lane == 0) myprep[sl] = PrepTile{b, g, t, n, nt};
-            const int pos0 = t * kTN;
-            const int nvalid = min(kTN, n - pos0);
+            const int pos0 = t * TN;
+            const int nvalid = min(TN, n - pos0);
 #pragma unroll
-            for (int k2 = 0; k2 < kLaneBoxes; ++k2) {
+            for (int k2 = 0; k2 < S::LANE_BOXES; ++k2) {
                 const int k = lane + 32 * k2;
                 if (k < nbox && k * R < nvalid)
-                    cp_async4(smem_addr(myids + sl * kTN + k),
+                    cp_async4(smem_addr(myids + sl * TN + k),
                               p.block_tables + static_cast<size_t>(b) * p.max_blocks + p.geom.block_of(pos0 + k * R));
             }
             cp_async_commit();
@@ -458,17 +464,17 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
             const int sl = static_cast<int>(j % kIdRing);
             const PrepTile pm = myprep[sl];
             const int pb_ = pm.b, pg = pm.g, pt = pm.t, pn = pm.n, pnt = pm.nt;
-            const int pos0 = pt * kTN;
-            const int nvalid = min(kTN, pn - pos0);
-            int slots[kLaneBoxes];
-            unsigned good[kLaneBoxes], badm[kLaneBoxes];
+            const int pos0 = pt * TN;
+            const int nvalid = min(TN, pn - pos0);
+            int slots[S::LANE_BOXES];
+            unsigned good[S::LANE_BOXES], badm[S::LANE_BOXES];
 #pragma unroll
-            for (int k2 = 0; k2 < kLaneBoxes; ++k2) {
+            for (int k2 = 0; k2 < S::LANE_BOXES; ++k2) {
                 const int k = lane + 32 * k2;
                 slots[k2] = -1;
                 bool bad = false;
                 if (k < nbox && k * R < nvalid) {
-                    const int id = myids[sl * kTN + k];
+                    const int id = myids[sl * TN + k];
                     if (id >= 0 && id < p.num_blocks)
                         slots[k2] = id * p.geom.block_size + p.geom.offset_of(pos0 + k * R);
                     else
@@ -478,20 +484,24 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
                 badm[k2] = __ballot_sync(kFull, bad);
             }
             // rows holding context positions: [0, nvalid), minus the boxes of ids outside the pool
-            unsigned long long vmask = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+            // (128-bit mask; a box never straddles its 64-bit word: R divides 64)
+            unsigned long long vm0 = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+            unsigned long long vm1 = 0ull;
+            if constexpr (TN == 128) vm1 = nvalid >= 128 ? ~0ull : nvalid > 64 ? ((1ull << (nvalid - 64)) - 1ull) : 0ull;
             unsigned nbad = 0, ngood = 0;
 #pragma unroll
-            for (int k2 = 0; k2 < kLaneBoxes; ++k2) {
+            for (int k2 = 0; k2 < S::LANE_BOXES; ++k2) {
                 nbad += __popc(badm[k2]);
                 ngood += __popc(good[k2]);
             }
             if (nbad) {  // rare: flagged, and those rows are masked
                 if (lane == 0) raise_err(p.err, PA_DEVERR_TABLE);
 #pragma unroll
-                for (int k2 = 0; k2 < kLaneBoxes; ++k2)
+                for (int k2 = 0; k2 < S::LANE_BOXES; ++k2)
                     for (unsigned m = badm[k2]; m; m &= m - 1) {
-                        const int k = 32 * k2 + __ffs(m) - 1;
-                        vmask &= ~(box_rows_mask << (k * R));
+                        const int r0 = (32 * k2 + __ffs(m) - 1) * R;
+                        if (TN == 64 || r0 < 64) vm0 &= ~(box_rows_mask << r0);
+                        else vm1 &= ~(box_rows_mask << (r0 - 64));
                     }
             }
             uint32_t bytes = ngood * 2u * box_bytes;
@@ -524,9 +534,9 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
                 m.b = pb_;
                 m.g = pg;
                 m.flags = flags;
-                m.all_valid = vmask == ~0ull;
-                m.valid[0] = vmask;
-                m.valid[1] = 0ull;
+                m.all_valid = vm0 == ~0ull && (TN == 64 || vm1 == ~0ull);
+                m.valid[0] = vm0;
+                m.valid[1] = vm1;
                 m.newrow = new_tok ? (pn - 1) - pos0 : -1;
                 m.pad = 0;
                 metas[stage] = m;
@@ -535,14 +545,14 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
             __syncwarp();
             const uint32_t kdst = smem_addr(st), vdst = kdst + S::TILE_BYTES;
 #pragma unroll
-            for (int k2 = 0; k2 < kLaneBoxes; ++k2) {
+            for (int k2 = 0; k2 < S::LANE_BOXES; ++k2) {
                 const int k = lane + 32 * k2;
                 if (slots[k2] >= 0) {
                     if constexpr (S::MMA) {
                         // one box per 64-column half, 128-byte rows, swizzled
 #pragma unroll
                         for (int hf = 0; hf < S::NH; ++hf) {
-                            const uint32_t o = hf * kSwHalf + k * R * 128;
+                            const uint32_t o = hf * S::SW_HALF + k * R * 128;
                             tma_load_3d(kdst + o, &p.tmap_k, 64 * hf, pg, slots[k2], full0 + 8 * stage);
                             tma_load_3d(vdst + o, &p.tmap_v, 64 * hf, pg, slots[k2], full0 + 8 * stage);
                         }
@@ -560,25 +570,25 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
                 const size_t row_off = (static_cast<size_t>(pb_) * p.Hkv + pg) * D;
                 if (lane == 0) {
                     if constexpr (S::MMA) {
-                        // row kTN of each half, copied in as it is (readers take phase 0 there)
+                        // row TN of each half, copied in as it is (readers take phase 0 there)
 #pragma unroll
                         for (int hf = 0; hf < S::NH; ++hf) {
-                            const uint32_t o = hf * kSwHalf + kTN * 128;
+                            const uint32_t o = hf * S::SW_HALF + TN * 128;
                             bulk_load(kdst + o, static_cast<const T *>(p.k_new) + row_off + 64 * hf, 128,
                                       full0 + 8 * stage);
                             bulk_load(vdst + o, static_cast<const T *>(p.v_new) + row_off + 64 * hf, 128,
                                       full0 + 8 * stage);
                         }
                     } else {
-                        bulk_load(kdst + kTN * D * 2, static_cast<const T *>(p.k_new) + row_off, D * 2,
+                        bulk_load(kdst + TN * D * 2, static_cast<const T *>(p.k_new) + row_off, D * 2,
                                   full0 + 8 * stage);
-                        bulk_load(vdst + kTN * D * 2, static_cast<const T *>(p.v_new) + row_off, D * 2,
+                        bulk_load(vdst + TN * D * 2, static_cast<const T *>(p.v_new) + row_off, D * 2,
                                   full0 + 8 * stage);
                     }
                 }
                 // ... and into the pool, at the slot of position pn - 1 (no copy in this launch
                 // reads that slot's row: the tile takes it from the spare row)
-                const int id = myids[sl * kTN + (pn - 1 - pos0) / R];  // its box's block
+                const int id = myids[sl * TN + (pn - 1 - pos0) / R];  // its box's block
                 constexpr int kChunks = D * 2 / 16;  // 16-byte chunks per row
                 if (id >= 0 && id < p.num_blocks && lane < 2 * kChunks) {
                     const long long slot = static_cast<long long>(id) * p.geom.block_size + p.geom.offset_of(pn - 1);
@@ -689,7 +699,6 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
             const int mflags = m.flags, mb = m.b, mg = m.g, mall = m.all_valid, mnew = m.newrow;
             const unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
             const uint32_t kb = smem_addr(st), vb = kb + S::TILE_BYTES;
-            const unsigned vrows = warp_rows_valid(m, cw);
 
             if (mflags & kFirst) {
                 const uint32_t *qs = reinterpret_cast<const uint32_t *>(st + 2 * S::TILE_BYTES);
@@ -703,63 +712,67 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
                 m_run = -INFINITY;
                 l_part = 0.f;
             }
-            // the row this lane addresses in ldmatrix: row lr of the warp's 8, or the spare row
-            // that holds the new token (copied in unswizzled: phase 0)
-            const int row0 = cw * kWPos + lr;
-            const int row = row0 == mnew ? kTN : row0;
-            const uint32_t rbase = static_cast<uint32_t>(row) * 128u;
-            const bool spare = row == kTN;
-            // 128-byte swizzle phase of this row in each half of K and V: (address >> 7) & 7
-            auto swz = [&](uint32_t a) -> uint32_t { return spare ? 0u : ((a >> 7) & 7u); };
-
-            // ---- S = Q K^T: this lane gets head gq at the warp's rows 2tq, 2tq + 1 ----
-            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {  // chunks 4q .. 4q + 3 (columns 32q .. 32q + 31)
-                uint32_t r4[4];
-                const uint32_t a = kb + (q >> 1) * kSwHalf + rbase;
-                ldsm_x4(a + (((4u * (q & 1) + lm) ^ swz(a)) << 4), r4);
-                mma_k16<E>(s0, qa[2 * q][0], qa[2 * q][1], r4[0], r4[1]);
-                mma_k16<E>(s1, qa[2 * q + 1][0], qa[2 * q + 1][1], r4[2], r4[3]);
-            }
-            const bool v0 = (vrows >> (2 * tq)) & 1u, v1 = (vrows >> (2 * tq + 1)) & 1u;
-            const float x0 = v0 ? (s0[0] + s1[0]) * p.scale_log2 : -INFINITY;
-            const float x1 = v1 ? (s0[1] + s1[1]) * p.scale_log2 : -INFINITY;
+            for (int sub = 0; sub < S::SUB; ++sub) {  // 64-row sub-tiles of the stage
+                const unsigned vrows = warp_rows_valid(m, cw, sub);
+                // the row this lane addresses in ldmatrix: row lr of the warp's 8, or the spare row
+                // that holds the new token (copied in unswizzled: phase 0)
+                const int row0 = sub * kTN + cw * kWPos + lr;
+                const int row = row0 == mnew ? S::TN : row0;
+                const uint32_t rbase = static_cast<uint32_t>(row) * 128u;
+                const bool spare = row == S::TN;
+                // 128-byte swizzle phase of this row in each half of K and V: (address >> 7) & 7
+                auto swz = [&](uint32_t a) -> uint32_t { return spare ? 0u : ((a >> 7) & 7u); };
 
-            // ---- online softmax (base 2) over the warp's 8 rows: a quad holds one head ----
-            float mt = fmaxf(x0, x1);
-            mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
-            mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
-            const float m_new = fmaxf(m_run, mt);
-            const float mu = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = fast_exp2(m_run - mu);
-            const float p0 = fast_exp2(x0 - mu), p1 = fast_exp2(x1 - mu);
-            m_run = m_new;
-            l_part = fmaf(l_part, alpha, p0 + p1);
-            // P^T as the B fragment of O^T += V^T P^T: the score fragment's layout as it stands
-            const uint32_t pb = E::pack2(p0, p1);
-            // the rescale factors of this lane's two O^T columns (heads 2tq, 2tq + 1)
-            const float al0 = __shfl_sync(kFull, alpha, 8 * tq), al1 = __shfl_sync(kFull, alpha, 8 * tq + 4);
-
-            // ---- O^T = alpha O^T + V^T P^T, V^T read transposed by ldmatrix; rows outside the
-            // context are zeroed in the V fragment (their stage bytes may hold anything, and
-            // 0 * NaN is NaN) ----
-            const uint32_t keep = mall ? 0xffffffffu : ((v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u));
+                // ---- S = Q K^T: this lane gets head gq at the warp's rows 2tq, 2tq + 1 ----
+                float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t r4[4];
-                const uint32_t a = vb + (q >> 1) * kSwHalf + rbase;
-                ldsm_x4_t(a + (((4u * (q & 1) + lm) ^ swz(a)) << 4), r4);
-#pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    float(&a)[4] = acc[2 * q + hb];
-                    a[0] *= al0;
-                    a[1] *= al1;
-                    a[2] *= al0;
-                    a[3] *= al1;
-                    mma_k8<E>(a, r4[2 * hb] & keep, r4[2 * hb + 1] & keep, pb);
+                for (int q = 0; q < D / 32; ++q) {  // chunks 4q .. 4q + 3 (columns 32q .. 32q + 31)
+                    uint32_t r4[4];
+                    const uint32_t a = kb + (q >> 1) * S::SW_HALF + rbase;
+                    ldsm_x4(a + (((4u * (q & 1) + lm) ^ swz(a)) << 4), r4);
+                    mma_k16<E>(s0, qa[2 * q][0], qa[2 * q][1], r4[0], r4[1]);
+                    mma_k16<E>(s1, qa[2 * q + 1][0], qa[2 * q + 1][1], r4[2], r4[3]);
                 }
-            }
+                const bool v0 = (vrows >> (2 * tq)) & 1u, v1 = (vrows >> (2 * tq + 1)) & 1u;
+                const float x0 = v0 ? (s0[0] + s1[0]) * p.scale_log2 : -INFINITY;
+                const float x1 = v1 ? (s0[1] + s1[1]) * p.scale_log2 : -INFINITY;
+
+                // ---- online softmax (base 2) over the warp's 8 rows: a quad holds one head ----
+                float mt = fmaxf(x0, x1);
+                mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 1));
+                mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 2));
+                const float m_new = fmaxf(m_run, mt);
+                const float mu = m_new == -INFINITY ? 0.f : m_new;
+                const float alpha = fast_exp2(m_run - mu);
+                const float p0 = fast_exp2(x0 - mu), p1 = fast_exp2(x1 - mu);
+                m_run = m_new;
+                l_part = fmaf(l_part, alpha, p0 + p1);
+                // P^T as the B fragment of O^T += V^T P^T: the score fragment's layout as it stands
+                const uint32_t pb = E::pack2(p0, p1);
+                // the rescale factors of this lane's two O^T columns (heads 2tq, 2tq + 1)
+                const float al0 = __shfl_sync(kFull, alpha, 8 * tq), al1 = __shfl_sync(kFull, alpha, 8 * tq + 4);
+
+                // ---- O^T = alpha O^T + V^T P^T, V^T read transposed by ldmatrix; rows outside the
+                // context are zeroed in the V fragment (their stage bytes may hold anything, and
+                // 0 * NaN is NaN) ----
+                const uint32_t keep = mall ? 0xffffffffu : ((v0 ? 0x0000ffffu : 0u) | (v1 ? 0xffff0000u : 0u));
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t r4[4];
+                    const uint32_t a = vb + (q >> 1) * S::SW_HALF + rbase;
+                    ldsm_x4_t(a + (((4u * (q & 1) + lm) ^ swz(a)) << 4), r4);
+#pragma unroll
+                    for (int hb = 0; hb < 2; ++hb) {
+                        float(&a)[4] = acc[2 * q + hb];
+                        a[0] *= al0;
+                        a[1] *= al1;
+                        a[2] *= al0;
+                        a[3] *= al1;
+                        mma_k8<E>(a, r4[2 * hb] & keep, r4[2 * hb + 1] & keep, pb);
+                    }
+                }
+            }  // sub-tiles
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * stage);
             if (++stage == NS) {
@@ -857,7 +870,7 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
                 uint64_t d2[G][S::CPL];
 #pragma unroll
                 for (int c = 0; c < S::CPL; ++c) {
-                    const uint4 kv = lds128(kb + (row == mnew ? kTN : row) * D * 2 + S::chunk(c, r, u) * 16);
+                    const uint4 kv = lds128(kb + (row == mnew ? S::TN : row) * D * 2 + S::chunk(c, r, u) * 16);
                     const uint64_t k0 = unpack_pair<E>(kv.x), k1 = unpack_pair<E>(kv.y);
                     const uint64_t k2 = unpack_pair<E>(kv.z), k3 = unpack_pair<E>(kv.w);
 #pragma unroll
@@ -921,7 +934,7 @@ __global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_k
             }
             auto pv_row = [&](int rl) {
                 const int row0 = cw * kWPos + rl;
-                const int row = row0 == mnew ? kTN : row0;
+                const int row = row0 == mnew ? S::TN : row0;
                 uint64_t v[S::NPV];
                 if constexpr (S::CPV == 8) {
                     const uint4 vv = lds128(vb + row * D * 2 + cc * 16);
