@@ -54,8 +54,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # profiles/decode_kernel_qwen3_06b_decode.md and profiles/prefill_tc_kernel_prefill_prefix.md
 # (layer 0 of the default workload; prefill_prefix). Each is valid only for the kernel sources it
 # was taken on, identified by their hash; after any change the bench reports null.
-DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_281_796_352,
-                  "sha256": "844a4d0c467a07b17dcb6bea04faeaea1e337e56c90e1105701cc0c0f169c30b"}
+DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_283_056_128,
+                  "sha256": "84cca68bf09e1acffded93d32205ce48842a3ddf1e963bc591175e3ea5b9d074"}
 PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 411_089_920,
                    "sha256": "d56841fd65495c1c9a79fd3c92669449ba16f74585a2c9c6b73af500664f8661"}
 
@@ -534,34 +534,37 @@ GROUP_SWEEP = ((4, 4, 128, 256, "bf16"), (7, 2, 64, 16, "f16"), (8, 2, 128, 256,
 
 
 def bench_group_sweep(torch, pa, dev, hbm) -> dict:
-    """pa_decode across GQA group sizes G = Hq / Hkv (G >= 4 runs the tensor-core consumers),
-    timed with an L2 flush between iterations."""
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    """pa_decode across GQA group sizes G = Hq / Hkv (G >= 4 runs the tensor-core consumers).
+    Like the main step: calls back to back on two layers whose pools alternate (each KV set is
+    larger than L2), CUDA events around each call, the median call reported."""
     res = {}
     for G, Hkv, D, bs, dt in GROUP_SWEEP:
         lens = np.random.default_rng(0).integers(100, 4096, size=256, endpoint=True)
-        c = W.decode_case(B=256, Hq=G * Hkv, Hkv=Hkv, D=D, block_size=bs, dtype=dt,
-                          context_lens=lens, seed=1)
-        L = DecodeLayer(torch, pa, c, dev)
-        run = lambda: pa.pa_decode(L.out, L.q, L.kc, L.vc, L.bt, L.cl, c.scale, workspace=L.ws)
-        for _ in range(3):
-            run()
-        ts = []
-        for _ in range(20):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            run()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        ms = statistics.median(ts)
+        layers = [DecodeLayer(torch, pa, W.decode_case(B=256, Hq=G * Hkv, Hkv=Hkv, D=D, block_size=bs,
+                                                       dtype=dt, context_lens=lens, seed=1 + l), dev)
+                  for l in range(2)]
+        c = layers[0].c
+
+        def run(L):
+            pa.pa_decode(L.out, L.q, L.kc, L.vc, L.bt, L.cl, L.c.scale, workspace=L.ws)
+
+        for i in range(4):
+            run(layers[i % 2])
+        n = 20
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize()
+        for i in range(n):
+            evs[i][0].record()
+            run(layers[i % 2])
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
         kv = kv_bytes(c.context_lens, c.Hkv, c.D)
         res[f"G{G}_Hkv{Hkv}_D{D}_bs{bs}_{dt}"] = {
             "us": ms * 1e3, "kv_bytes": kv, "GB_per_s": kv / (ms * 1e-3) / 1e9,
             "frac_of_hbm": kv / (ms * 1e-3) / 1e9 / hbm,
             "consumers": "tensor-core fragments" if G >= 4 else "fp32"}
-        del L
+        del layers
         torch.cuda.empty_cache()
     return res
 
