@@ -18,7 +18,6 @@ from tests.gpu_util import TOL, bits, err_buf, f64, i32, max_abs, to_dev, worksp
 pytestmark = pytest.mark.gpu
 
 BUCKET, NB, BS, MAXB = 64, 4096, 16, 64  # 64 rows x 64 blocks fit the pool
-Hq, Hkv, D, DT = 16, 8, 128, "bf16"
 
 
 @pytest.fixture(scope="module")
@@ -26,7 +25,7 @@ def orc():
     return oracle.get()
 
 
-def _batch(n_real, seed):
+def _batch(n_real, seed, Hq, Hkv, D, DT):
     rng = np.random.default_rng([seed, 5])
     ctx = np.zeros(BUCKET, np.int64)
     ctx[:n_real] = rng.integers(1, MAXB * BS, size=n_real)
@@ -34,8 +33,12 @@ def _batch(n_real, seed):
                          num_blocks=NB, max_blocks_per_seq=MAXB, seed=seed)
 
 
-def test_padded_bucket_graph_replays(orc):
-    c0 = _batch(BUCKET, 1)
+# the fp32 consumers (group 2) and the tensor-core ones (the Qwen2.5 head shape, group 7); the
+# step as two calls (store, then decode) and as the fused call
+@pytest.mark.parametrize("Hq,Hkv,D,DT", [(16, 8, 128, "bf16"), (14, 2, 64, "f16")])
+@pytest.mark.parametrize("fused", [False, True])
+def test_padded_bucket_graph_replays(orc, Hq, Hkv, D, DT, fused):
+    c0 = _batch(BUCKET, 1, Hq, Hkv, D, DT)
     bufs = {"q": to_dev(c0.q, DT), "kn": to_dev(c0.k_new, DT), "vn": to_dev(c0.v_new, DT),
             "kc": to_dev(c0.k_cache, DT), "vc": to_dev(c0.v_cache, DT),
             "bt": i32(c0.block_tables), "cl": i32(c0.context_lens), "sm": i32(c0.slot_mapping)}
@@ -44,6 +47,10 @@ def test_padded_bucket_graph_replays(orc):
     err = err_buf()
 
     def body():
+        if fused:
+            pa.pa_store_decode(out, bufs["q"], bufs["kn"], bufs["vn"], bufs["kc"], bufs["vc"],
+                               bufs["bt"], bufs["cl"], c0.scale, workspace=ws, err=err)
+            return
         pa.pa_store_kv(bufs["kn"], bufs["vn"], bufs["kc"], bufs["vc"], bufs["sm"], err=err)
         pa.pa_decode(out, bufs["q"], bufs["kc"], bufs["vc"], bufs["bt"], bufs["cl"], c0.scale,
                      workspace=ws, err=err)
@@ -55,7 +62,7 @@ def test_padded_bucket_graph_replays(orc):
         body()
 
     for n_real, seed in [(40, 2), (BUCKET, 3), (1, 4), (40, 2)]:
-        c = _batch(n_real, seed)
+        c = _batch(n_real, seed, Hq, Hkv, D, DT)
         src = {"q": c.q, "kn": c.k_new, "vn": c.v_new, "kc": c.k_cache, "vc": c.v_cache}
         for key, a in src.items():
             bufs[key].copy_(to_dev(a, DT))
