@@ -111,9 +111,11 @@ def _i32(t: torch.Tensor | None, name: str):
     return _ptr(t)
 
 
-def _stream(stream) -> int | None:
+def _stream(stream, ref: torch.Tensor) -> int | None:
+    """The raw stream handle: the given stream, else the current stream of ref's device (read
+    straight from torch's stream registry: building a torch Stream object costs ~3 us a call)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        return torch._C._cuda_getCurrentRawStream(ref.get_device())
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
@@ -135,7 +137,7 @@ def pa_store_kv(k, v, k_cache, v_cache, slot_mapping, err=None, stream=None) -> 
         raise TypeError("k, v and the pools must share a dtype")
     _check("pa_store_kv", load().pa_store_kv(
         _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _i32(slot_mapping, "slot_mapping"), T, NB,
-        bs, Hkv, D, dt, _i32(err, "err"), _stream(stream)))
+        bs, Hkv, D, dt, _i32(err, "err"), _stream(stream, k)))
 
 
 def pa_decode_workspace_size(B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int,
@@ -159,7 +161,7 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float
     _check("pa_decode", load().pa_decode(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _i32(block_tables, "block_tables"), maxb,
         _i32(context_lens, "context_lens"), B, Hq, Hkv, D, bs, NB, float(scale), dt,
-        _ptr(workspace), ws_bytes, _i32(err, "err"), _stream(stream)))
+        _ptr(workspace), ws_bytes, _i32(err, "err"), _stream(stream, q)))
 
 
 def pa_store_decode(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
@@ -181,7 +183,7 @@ def pa_store_decode(out, q, k_new, v_new, k_cache, v_cache, block_tables, contex
         _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
         _i32(block_tables, "block_tables"), maxb, _i32(context_lens, "context_lens"), B, Hq, Hkv,
         D, bs, NB, float(scale), dt, _ptr(workspace), ws_bytes, _i32(err, "err"),
-        _stream(stream)))
+        _stream(stream, q)))
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
@@ -200,7 +202,7 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scal
     _check("pa_decode_noalloc", load().pa_decode_noalloc(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _i32(block_tables, "block_tables"),
         block_tables.shape[1], _i32(context_lens, "context_lens"), B, Hq, Hkv, D, bs, NB,
-        float(scale), dt, _i32(err, "err"), _stream(stream)))
+        float(scale), dt, _i32(err, "err"), _stream(stream, q)))
 
 
 def pa_prefill_varlen(out, q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k,
@@ -232,7 +234,7 @@ def pa_prefill_varlen(out, q, k, v, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k
         _ptr(out), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache),
         _i32(cu_seqlens_q, "cu_seqlens_q"), _i32(cu_seqlens_k, "cu_seqlens_k"), S, Tq, total_k,
         int(max_seqlen_q), int(max_seqlen_k), _i32(block_tables, "block_tables"), maxb, Hq, Hkv, D,
-        bs, NB, float(scale), int(bool(causal)), dt, _i32(err, "err"), _stream(stream)))
+        bs, NB, float(scale), int(bool(causal)), dt, _i32(err, "err"), _stream(stream, q)))
 
 
 # ---------------------------------------------------------------------------------------------

@@ -1135,6 +1135,34 @@ bool encode_pool(CUtensorMap *m, const void *pool, pa_dtype dt, int D, int Hkv, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// encode_pool through a small per-thread cache: a tensor map is a pure function of its
+// arguments, so a hit is exact (also after a pool is freed and another one takes its address)
+bool encode_pool_cached(CUtensorMap *m, const void *pool, pa_dtype dt, int D, int Hkv, long long slots,
+                        int box_rows, bool swizzled) {
+    struct Entry {
+        const void *pool;
+        long long slots;
+        int dt, D, Hkv, box_rows, swizzled, valid;
+        CUtensorMap map;
+    };
+    constexpr int kEntries = 8;
+    thread_local Entry cache[kEntries] = {};
+    thread_local int next = 0;
+    for (int i = 0; i < kEntries; ++i) {
+        const Entry &e = cache[i];
+        if (e.valid && e.pool == pool && e.slots == slots && e.dt == static_cast<int>(dt) && e.D == D &&
+            e.Hkv == Hkv && e.box_rows == box_rows && e.swizzled == static_cast<int>(swizzled)) {
+            *m = e.map;
+            return true;
+        }
+    }
+    if (!encode_pool(m, pool, dt, D, Hkv, slots, box_rows, swizzled)) return false;
+    Entry &e = cache[next];
+    next = (next + 1) % kEntries;
+    e = Entry{pool, slots, static_cast<int>(dt), D, Hkv, box_rows, static_cast<int>(swizzled), 1, *m};
+    return true;
+}
+
 template <int D, int G>
 constexpr int stages_for() {
     const int budget = kSmemPerSm / ctas_per_sm(D, G) - 1024;
@@ -1227,8 +1255,8 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     const long long slots = static_cast<long long>(a.num_blocks) * a.block_size;
     const int G = a.Hq / a.Hkv;
     const bool sw = G >= kMmaMinGroup;  // tensor-core consumers read swizzled tiles
-    if (!encode_pool(&prm.tmap_k, a.k_cache, a.dtype, a.D, a.Hkv, slots, R, sw) ||
-        !encode_pool(&prm.tmap_v, a.v_cache, a.dtype, a.D, a.Hkv, slots, R, sw))
+    if (!encode_pool_cached(&prm.tmap_k, a.k_cache, a.dtype, a.D, a.Hkv, slots, R, sw) ||
+        !encode_pool_cached(&prm.tmap_v, a.v_cache, a.dtype, a.D, a.Hkv, slots, R, sw))
         return cudaErrorInvalidValue;
     prm.q = a.q;
     prm.k_new = a.k_new;
