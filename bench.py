@@ -184,6 +184,23 @@ class Clocks:
 # CPU oracle timing (the baseline and the reference arm)
 # ---------------------------------------------------------------------------------------------
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, else implementer/part ids), with the
+    core count."""
+    name = ""
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+        for key in ("model name", "Model name", "CPU part"):
+            hits = [l.split(":", 1)[1].strip() for l in info if l.startswith(key)]
+            if hits:
+                name = f"{key}: {hits[0]}"
+                break
+    except OSError:
+        pass
+    import platform
+    return f"{platform.machine()}, {os.cpu_count()} cores" + (f", {name}" if name else "")
+
+
 def oracle_decode_rate(case, budget_s: float = 12.0, threads: int = 0) -> dict:
     """Time the oracle's decode on a bounded sample of the case's sequences (after applying the
     step's store, as the GPU step does), growing the sample until ~budget_s of work."""
@@ -202,10 +219,18 @@ def oracle_decode_rate(case, budget_s: float = 12.0, threads: int = 0) -> dict:
         if dt >= budget_s / 4 or n == case.B:
             break
         n = min(case.B, max(n + 1, int(n * min(8.0, (budget_s / 4) / max(dt, 1e-3)))))
+    reps = 1
+    if dt < budget_s / 4:  # the whole case is quick: repeat it to time a meaningful span
+        reps = int(min(1000, max(1, (budget_s / 4) / max(dt, 1e-4))))
+        t = time.perf_counter()
+        for _ in range(reps):
+            orc.decode(case.q[rows], kc, vc, case.block_tables[rows], case.context_lens[rows],
+                       scale=case.scale, dtype=case.dtype, threads=threads)
+        dt = (time.perf_counter() - t) / reps
     nbytes = kv_bytes(case.context_lens[rows], case.Hkv, case.D)
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": orc.max_threads(), "kind": "oracle",
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": min(threads, orc.max_threads()), "kind": "oracle",
             "sample": f"{n} of {case.B} sequences of {case.name} (store applied, fp64 decode), "
-                      f"{nbytes / 1e6:.1f} MB of KV in {dt:.2f} s",
+                      f"{nbytes / 1e6:.1f} MB of KV in {dt:.4f} s" + (f", mean of {reps} runs" if reps > 1 else ""),
             "seconds": dt, "seqs": int(n), "rows": rows}
 
 
@@ -435,6 +460,18 @@ def run_gpu(args, ws_, rank, local):
         r.pop("rows")
         r.pop("seqs")
         cpu = r
+        cpu["cpu_model"] = cpu_model()
+        # beside it: the oracle on one thread, and on the two small decode configurations
+        one = oracle_decode_rate(layers[0].c, budget_s=4.0, threads=1)
+        cpu["one_thread"] = {"value": one["value"], "unit": "GB/s", "sample": one["sample"]}
+        small = {}
+        for name in ("tiny", "qwen25_05b_decode"):
+            sc = W.make(name)
+            a = oracle_decode_rate(sc, budget_s=2.0)
+            b = oracle_decode_rate(sc, budget_s=2.0, threads=1)
+            small[name] = {"all_cores_GB_per_s": a["value"], "one_thread_GB_per_s": b["value"],
+                           "sample_all_cores": a["sample"], "sample_one_thread": b["sample"]}
+        cpu["small_configs"] = small
 
     if rank != 0:
         if dist is not None:
