@@ -196,3 +196,23 @@ def test_many_tiles_per_cta_sampled(orc, G, Hkv, D, bs, dt):
     c = W.decode_case(B=256, Hq=G * Hkv, Hkv=Hkv, D=D, block_size=bs, dtype=dt, context_lens=lens,
                       seed=12)
     _sampled_full_size(orc, None, nsample=8, case=c)
+
+
+@pytest.mark.parametrize("G,Hkv,D,bs,dt", [(8, 2, 128, 16, "bf16"), (7, 2, 64, 256, "f16")])
+def test_batch_larger_than_a_cta_tensor_core_path(orc, G, Hkv, D, bs, dt):
+    """More sequences than a CTA has threads (320 on the tensor-core path): the start-up scan
+    over the context lengths runs in chunks. Zero-length sequences are mixed in."""
+    rng = np.random.default_rng(21)
+    lens = rng.integers(1, 600, size=700, endpoint=True)
+    lens[rng.choice(700, size=40, replace=False)] = 0
+    c = W.decode_case(B=700, Hq=G * Hkv, Hkv=Hkv, D=D, block_size=bs, dtype=dt, context_lens=lens,
+                      seed=22)
+    run = DecodeRun(c)
+    out = f64(run.step())
+    assert int(run.err.item()) == 0
+    kc_ref, vc_ref = orc.store_kv(c.k_new, c.v_new, c.k_cache, c.v_cache, c.slot_mapping)
+    assert np.array_equal(bits(run.kc), kc_ref) and np.array_equal(bits(run.vc), vc_ref)
+    zero = np.flatnonzero(lens == 0)
+    assert not out[zero].any()
+    rows = sorted(set(rng.choice(700, size=24, replace=False).tolist() + [int(zero[0])]))
+    assert max_abs(out[rows], _reference(orc, c, kc_ref, vc_ref, rows)) <= TOL[dt]
