@@ -66,6 +66,11 @@ constexpr bool use_mma() { return G >= kMmaMinGroup; }
 // persistent CTAs per SM: two (two TMA streams, 16 consumer warps) when the consumers fit the
 // halved register file, else one
 __host__ __device__ constexpr int ctas_per_sm(int D, int G) { return G < kMmaMinGroup ? 2 : 1; }
+// The D = 64 tensor-core kernels also come with two CTAs per SM (half the stages each, twice the
+// producers per SM): faster on large batches, slower on small ones, where the longer pipeline
+// start of each CTA is not paid back. Chosen per launch from an upper bound of the stages per SM.
+constexpr int kWideMinStagesPerSm = 32;
+__host__ __device__ constexpr bool has_wide(int D, int G) { return G >= kMmaMinGroup && D == 64; }
 // producer warps (alternate tiles): two keep the light tensor-core consumers fed; with the fp32
 // consumers one suffices and a second only takes issue slots from them
 __host__ __device__ constexpr int producers_for(int D, int G) { return G < kMmaMinGroup ? 1 : 2; }
@@ -106,10 +111,10 @@ struct DecodeParams {
     float scale_log2;
 };
 
-template <int D, int G>
+template <int D, int G, int CPS_ = ctas_per_sm(D, G)>
 struct Shape {
     static constexpr int NCH = D / 8;  // 16-byte chunks per row
-    static constexpr int CPS = ctas_per_sm(D, G);
+    static constexpr int CPS = CPS_;
     // QK elements per lane: keeps the query registers (G * E) at 32 with two CTAs per SM,
     // at 64 with one
     static constexpr int E_RAW = CPS == 2 ? (G == 1 ? 32 : G == 2 ? 16 : 8) : (G <= 4 ? 16 : 8);
@@ -157,11 +162,12 @@ struct Shape {
     }
 };
 
-template <int D, int G>
+template <int D, int G, int CPS>
 constexpr int fixed_smem() {
     // + metas, barriers, scan scratch (1 KB), the slack that aligns the ring (1 KB) and the
     // producer's ring of prepared tiles
-    return Shape<D, G>::RED_BYTES + Shape<D, G>::SCRATCH_BYTES + 2048 + producers_for(D, G) * kIdRing * (Shape<D, G>::TN * 4 + 32);
+    using S = Shape<D, G, CPS>;
+    return S::RED_BYTES + S::SCRATCH_BYTES + 2048 + producers_for(D, G) * kIdRing * (S::TN * 4 + 32);
 }
 
 // All 32 lanes wait for the phase, then the warp reconverges; false (for every lane) if the wait
@@ -243,9 +249,9 @@ __device__ long long block_sum(long long v, long long *red) {
     return t;
 }
 
-template <int D, int G, class E>
-__global__ void __launch_bounds__(threads_for(D, G), ctas_per_sm(D, G)) decode_kernel(const __grid_constant__ DecodeParams p) {
-    using S = Shape<D, G>;
+template <int D, int G, class E, int CPS>
+__global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __grid_constant__ DecodeParams p) {
+    using S = Shape<D, G, CPS>;
     constexpr int kProducers = producers_for(D, G), kThreads = threads_for(D, G);
     using T = typename E::T;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1163,24 +1169,24 @@ bool encode_pool_cached(CUtensorMap *m, const void *pool, pa_dtype dt, int D, in
     return true;
 }
 
-template <int D, int G>
+template <int D, int G, int CPS>
 constexpr int stages_for() {
-    const int budget = kSmemPerSm / ctas_per_sm(D, G) - 1024;
+    const int budget = kSmemPerSm / CPS - 1024;
     // A multiple of the producer count, so that each stage belongs to one producer. (A stage that
     // alternated between producers could not be waited on by parity: a producer cannot tell
     // whether the other has armed the stage's previous phase yet, and a barrier two phases behind
     // has the parity of the phase it waits for.)
     constexpr int np = producers_for(D, G);
-    const int s = (budget - fixed_smem<D, G>()) / Shape<D, G>::STAGE_BYTES / np * np;
+    const int s = (budget - fixed_smem<D, G, CPS>()) / Shape<D, G, CPS>::STAGE_BYTES / np * np;
     return s < kMaxStages / np * np ? s : kMaxStages / np * np;
 }
 
-template <int D, int G, class E>
+template <int D, int G, class E, int CPS = ctas_per_sm(D, G)>
 cudaError_t launch_typed(DecodeParams &prm, cudaStream_t stream) {
-    static_assert(stages_for<D, G>() >= 2, "the ring needs two stages");
-    prm.stages = stages_for<D, G>();
-    const int smem = prm.stages * Shape<D, G>::STAGE_BYTES + fixed_smem<D, G>();
-    auto kern = decode_kernel<D, G, E>;
+    static_assert(stages_for<D, G, CPS>() >= 2, "the ring needs two stages");
+    prm.stages = stages_for<D, G, CPS>();
+    const int smem = prm.stages * Shape<D, G, CPS>::STAGE_BYTES + fixed_smem<D, G, CPS>();
+    auto kern = decode_kernel<D, G, E, CPS>;
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1190,7 +1196,7 @@ cudaError_t launch_typed(DecodeParams &prm, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured[dev] = smem;
     }
-    const int P = device_sm_count() * ctas_per_sm(D, G);
+    const int P = device_sm_count() * CPS;
     if (P > kMergeMaxCtas) return cudaErrorInvalidConfiguration;
     // both kernels launch as programmatic dependents of what precedes them in the stream: a
     // launch overlaps the tail of the grid before it, and each kernel waits on the grid
@@ -1217,30 +1223,48 @@ cudaError_t launch_typed(DecodeParams &prm, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D, G, E>, prm);
 }
 
+template <int D, int G, class E>
+cudaError_t launch_group(bool wide, DecodeParams &prm, cudaStream_t stream) {
+    if constexpr (has_wide(D, G))
+        if (wide) return launch_typed<D, G, E, 2>(prm, stream);
+    return launch_typed<D, G, E>(prm, stream);
+}
+
 template <int D, class E>
-cudaError_t dispatch_group(int G, DecodeParams &prm, cudaStream_t stream) {
+cudaError_t dispatch_group(int G, bool wide, DecodeParams &prm, cudaStream_t stream) {
     switch (G) {
-        case 1: return launch_typed<D, 1, E>(prm, stream);
-        case 2: return launch_typed<D, 2, E>(prm, stream);
-        case 3: return launch_typed<D, 3, E>(prm, stream);
-        case 4: return launch_typed<D, 4, E>(prm, stream);
-        case 5: return launch_typed<D, 5, E>(prm, stream);
-        case 6: return launch_typed<D, 6, E>(prm, stream);
-        case 7: return launch_typed<D, 7, E>(prm, stream);
-        case 8: return launch_typed<D, 8, E>(prm, stream);
+        case 1: return launch_group<D, 1, E>(wide, prm, stream);
+        case 2: return launch_group<D, 2, E>(wide, prm, stream);
+        case 3: return launch_group<D, 3, E>(wide, prm, stream);
+        case 4: return launch_group<D, 4, E>(wide, prm, stream);
+        case 5: return launch_group<D, 5, E>(wide, prm, stream);
+        case 6: return launch_group<D, 6, E>(wide, prm, stream);
+        case 7: return launch_group<D, 7, E>(wide, prm, stream);
+        case 8: return launch_group<D, 8, E>(wide, prm, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
+// CTAs per SM of a launch: the kernel's own, or two for the D = 64 tensor-core kernels when the
+// batch may give each SM at least kWideMinStagesPerSm stages (an upper bound: every sequence at
+// the table's full length)
+int launch_ctas_per_sm(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int block_size,
+                       bool allow_wide) {
+    const int G = Hq / Hkv;
+    if (!allow_wide || !has_wide(D, G)) return G < kMmaMinGroup ? 2 : 1;
+    const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+    const long long stages = static_cast<long long>(B) * Hkv * ((max_ctx + 2 * kTN - 1) / (2 * kTN));
+    return stages >= static_cast<long long>(kWideMinStagesPerSm) * device_sm_count() ? 2 : 1;
+}
+
 }  // namespace
 
-DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int block_size) {
-    (void)B;
-    (void)max_blocks_per_seq;
-    (void)block_size;
+DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int block_size,
+                       bool allow_wide) {
     DecodePlan plan{};
     const int G = Hq / Hkv;
-    const size_t P = static_cast<size_t>(device_sm_count()) * ctas_per_sm(D, G);
+    const size_t P = static_cast<size_t>(device_sm_count()) *
+                     launch_ctas_per_sm(B, Hq, Hkv, D, max_blocks_per_seq, block_size, allow_wide);
     const size_t part = P * 2 * G * (D + 2) * sizeof(float);
     plan.ws_bytes = (part + 255) / 256 * 256 + P * sizeof(SegRecord);
     return plan;
@@ -1266,7 +1290,8 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     prm.block_tables = a.block_tables;
     prm.context_lens = a.context_lens;
     prm.out = a.out;
-    const size_t P = static_cast<size_t>(device_sm_count()) * ctas_per_sm(a.D, G);
+    const int cps = launch_ctas_per_sm(a.B, a.Hq, a.Hkv, a.D, a.max_blocks, a.block_size, a.allow_wide);
+    const size_t P = static_cast<size_t>(device_sm_count()) * cps;
     const size_t part = P * 2 * G * (a.D + 2) * sizeof(float);
     prm.part = static_cast<float *>(a.workspace);
     prm.rec = reinterpret_cast<SegRecord *>(static_cast<char *>(a.workspace) + (part + 255) / 256 * 256);
@@ -1281,11 +1306,12 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     prm.geom.block_size = a.block_size;
     prm.geom.shift = log2_if_pow2(a.block_size);
     prm.scale_log2 = a.scale * kLog2e;
+    const bool wide = cps == 2 && has_wide(a.D, G);
     if (a.D == 128)
-        return a.dtype == PA_BF16 ? dispatch_group<128, BF16>(G, prm, stream)
-                                  : dispatch_group<128, F16>(G, prm, stream);
-    return a.dtype == PA_BF16 ? dispatch_group<64, BF16>(G, prm, stream)
-                              : dispatch_group<64, F16>(G, prm, stream);
+        return a.dtype == PA_BF16 ? dispatch_group<128, BF16>(G, wide, prm, stream)
+                                  : dispatch_group<128, F16>(G, wide, prm, stream);
+    return a.dtype == PA_BF16 ? dispatch_group<64, BF16>(G, wide, prm, stream)
+                              : dispatch_group<64, F16>(G, wide, prm, stream);
 }
 
 }  // namespace pa

@@ -45,7 +45,8 @@ extern "C" pa_status pa_decode_noalloc(void *out, const void *q, const void *k_c
     // pa_decode checks every argument and returns PA_ERR_WORKSPACE when these sizes need more
     // scratch than the fixed array holds. The partial results it keeps there are written before
     // they are read, so nothing has to be cleared between calls.
-    return pa_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, B,
-                     Hq, Hkv, D, block_size, num_blocks, scale, dtype, scratch,
-                     PA_DECODE_NOALLOC_SCRATCH_BYTES, err, stream);
+    // (one CTA per SM for every shape: the fixed scratch is sized for that)
+    return pa::decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, B,
+                            Hq, Hkv, D, block_size, num_blocks, scale, dtype, scratch,
+                            PA_DECODE_NOALLOC_SCRATCH_BYTES, err, stream, false);
 }

@@ -75,11 +75,14 @@ size_t pa_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_blocks_pe
     return pa::plan_decode(B, Hq, Hkv, D, max_blocks_per_seq, block_size).ws_bytes;
 }
 
-pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
-                    const int32_t *block_tables, int max_blocks_per_seq,
-                    const int32_t *context_lens, int B, int Hq, int Hkv, int D, int block_size,
-                    int num_blocks, float scale, pa_dtype dtype, void *workspace,
-                    size_t workspace_bytes, int32_t *err, cudaStream_t stream) {
+}  // extern "C"
+
+namespace pa {
+pa_status decode_entry(void *out, const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                       int B, int Hq, int Hkv, int D, int block_size, int num_blocks, float scale,
+                       pa_dtype dtype, void *workspace, size_t workspace_bytes, int32_t *err,
+                       cudaStream_t stream, bool allow_wide) {
     if (!dtype_ok(dtype)) return PA_ERR_DTYPE;
     if (B < 0 || max_blocks_per_seq < 0 || block_size < 1 || num_blocks < 0) return PA_ERR_SHAPE;
     pa_status st = check_heads(Hq, Hkv, D);
@@ -93,14 +96,28 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_UNSUPPORTED;
     if (static_cast<long long>(num_blocks) * block_size > INT_MAX) return PA_ERR_UNSUPPORTED;
-    const pa::DecodePlan plan = pa::plan_decode(B, Hq, Hkv, D, max_blocks_per_seq, block_size);
+    const pa::DecodePlan plan = pa::plan_decode(B, Hq, Hkv, D, max_blocks_per_seq, block_size, allow_wide);
     if (plan.ws_bytes > 0 && (!workspace || workspace_bytes < plan.ws_bytes || !aligned16(workspace)))
         return PA_ERR_WORKSPACE;
     pa::DecodeArgs a{out,  q,         k_cache,           v_cache,    block_tables,
                      context_lens, B, Hq,                Hkv,        D,
                      max_blocks_per_seq,  block_size, num_blocks, scale, dtype,
                      workspace,    err};
+    a.allow_wide = allow_wide;
     return from_cuda(pa::launch_decode(a, plan, stream));
+}
+}  // namespace pa
+
+extern "C" {
+
+pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *context_lens, int B, int Hq, int Hkv, int D, int block_size,
+                    int num_blocks, float scale, pa_dtype dtype, void *workspace,
+                    size_t workspace_bytes, int32_t *err, cudaStream_t stream) {
+    return pa::decode_entry(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, B,
+                            Hq, Hkv, D, block_size, num_blocks, scale, dtype, workspace,
+                            workspace_bytes, err, stream, true);
 }
 
 pa_status pa_store_decode(void *out, const void *q, const void *k_new, const void *v_new,

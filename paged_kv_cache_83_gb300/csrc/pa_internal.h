@@ -26,7 +26,10 @@ cudaError_t launch_store_kv(const StoreArgs &a, cudaStream_t stream);
 struct DecodePlan {
     size_t ws_bytes;  // scratch: per SM two partial results and one record
 };
-DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int block_size);
+// allow_wide: the D = 64 tensor-core kernels may run two CTAs per SM on large batches (the
+// launch and its workspace differ); the no-alloc entry point keeps one
+DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int block_size,
+                       bool allow_wide = true);
 
 struct DecodeArgs {
     void *out;
@@ -38,8 +41,16 @@ struct DecodeArgs {
     void *workspace;
     int32_t *err;
     const void *k_new = nullptr, *v_new = nullptr;  // fused store + decode: new rows [B, Hkv, D]
+    bool allow_wide = true;                           // see plan_decode
 };
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
+// pa_decode with the choice of allow_wide (pa_decode: allowed; pa_decode_noalloc: not, so that
+// its fixed scratch covers the same shapes whatever the batch)
+pa_status decode_entry(void *out, const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                       int B, int Hq, int Hkv, int D, int block_size, int num_blocks, float scale,
+                       pa_dtype dtype, void *workspace, size_t workspace_bytes, int32_t *err,
+                       cudaStream_t stream, bool allow_wide);
 
 // ------------------------------------------------------------------------------------------
 struct PrefillArgs {

@@ -216,3 +216,33 @@ def test_batch_larger_than_a_cta_tensor_core_path(orc, G, Hkv, D, bs, dt):
     assert not out[zero].any()
     rows = sorted(set(rng.choice(700, size=24, replace=False).tolist() + [int(zero[0])]))
     assert max_abs(out[rows], _reference(orc, c, kc_ref, vc_ref, rows)) <= TOL[dt]
+
+
+@pytest.mark.parametrize("G,dt", [(7, "f16"), (4, "bf16")])
+def test_two_ctas_per_sm_choice_elementwise(orc, G, dt):
+    """D = 64 tensor-core kernels run two CTAs per SM when the table width allows many stages per
+    SM (an upper bound: every sequence at the full width). Short real contexts in a wide table
+    take that choice while every row stays cheap to check against the oracle; the fused call
+    must give the same bits."""
+    rng = np.random.default_rng(31)
+    lens = rng.integers(1, 300, size=160, endpoint=True)
+    c = W.decode_case(B=160, Hq=2 * G, Hkv=2, D=64, block_size=16, dtype=dt, context_lens=lens,
+                      seed=32, max_blocks_per_seq=256)
+    _check_full(orc, c)
+    out, *_ = _fused_step(c)
+    run = DecodeRun(c)
+    assert torch.equal(out.view(torch.int16), run.step().view(torch.int16))
+
+
+def _fused_step(c):
+    kc, vc = to_dev(c.k_cache, c.dtype), to_dev(c.v_cache, c.dtype)
+    q = to_dev(c.q, c.dtype)
+    out = torch.empty_like(q)
+    err = err_buf()
+    pa.pa_store_decode(out, q, to_dev(c.k_new, c.dtype), to_dev(c.v_new, c.dtype), kc, vc,
+                       i32(c.block_tables), i32(c.context_lens), c.scale,
+                       workspace=workspace(c.B, c.Hq, c.Hkv, c.D, c.max_blocks_per_seq, c.block_size),
+                       err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return out, kc, vc
