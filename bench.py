@@ -54,8 +54,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # profiles/decode_kernel_qwen3_06b_decode.md and profiles/prefill_tc_kernel_prefill_prefix.md
 # (layer 0 of the default workload; prefill_prefix). Each is valid only for the kernel sources it
 # was taken on, identified by their hash; after any change the bench reports null.
-DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_282_662_400,
-                  "sha256": "dd5172277d897ab850f264a4fa34442a5665ec0f60b67f6fa1a62db71e29eb07"}
+DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_283_083_776,
+                  "sha256": "572363a1d7f958faabcdce21184aa229a9bfdda5ea6448d02f69d18911a5104a"}
 PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 411_290_112,
                    "sha256": "d7c18ebd78d322441abf0c57504a005c05546febc828c969fb144728954fb6a3"}
 
