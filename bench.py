@@ -12,8 +12,9 @@ steps per second per layer. The same line carries:
 
 * ``roofline``: the step's call (split kernel + merge) timed alone with CUDA events inside
   the timed region, against the measured copy bandwidth;
-* ``e2e``: the same metric when every step also copies its inputs from pinned host memory and
-  reads the output back, synchronising each step (the pool stays resident, as in an engine);
+* ``e2e``: the same metric through the C-ABI's host-buffer call (pa_store_decode_host): every
+  step copies its inputs from pinned host memory and reads the output back, synchronising each
+  step (the pool stays resident, as in an engine);
 * ``cpu_baseline``: the fp64 CPU oracle on a bounded sample of the same workload, on the
   host's cores;
 * ``rows``: the other rows of the path measured the same way: the same step as two calls
@@ -387,47 +388,70 @@ def run_gpu(args, ws_, rank, local):
     traffic = traffic_of(DECODE_TRAFFIC)
 
     # ---- e2e: inputs from pinned host memory each step, output read back each step ----
+    # through the C-ABI's host-buffer entry (pa_store_decode_host): the library queues one copy
+    # per input into its workspace, the fused store + decode, and the copy of the output back
     L = layers[0]
-    # the step's inputs travel as one pinned buffer and one copy (q, new K/V, tables, lengths at
-    # 256-byte aligned offsets), as an engine would stage them
-    parts = (L.q, L.k_new, L.v_new, L.bt, L.cl)
-    offs, total = [], 0
-    for x in parts:
-        offs.append(total)
-        total += (x.numel() * x.element_size() + 255) // 256 * 256
-    h_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
-    d_buf = torch.empty(total, dtype=torch.uint8, device=dev)
-    d_in = []
-    for x, o in zip(parts, offs):
+    c = L.c
+    # the step's inputs sit in one pinned buffer at the library's packed offsets, as an engine's
+    # scheduler would write them, so the call moves them in one copy
+    h_offs, h_total = pa.pa_store_decode_host_layout(c.B, c.Hq, c.Hkv, c.D, c.max_blocks_per_seq)
+    h_pack = torch.zeros(h_total, dtype=torch.uint8).pin_memory()
+    h_in = []
+    for x, o in zip((L.q, L.k_new, L.v_new, L.bt, L.cl), h_offs):
         nb_ = x.numel() * x.element_size()
-        h_buf[o:o + nb_].copy_(x.contiguous().cpu().view(-1).view(torch.uint8))
-        d_in.append(d_buf[o:o + nb_].view(x.dtype).view(x.shape))
+        v = h_pack[o:o + nb_].view(x.dtype).view(x.shape)
+        v.copy_(x.cpu())
+        h_in.append(v)
     h_out = torch.empty(L.out.shape, dtype=L.out.dtype).pin_memory()
-    h2d = total
+    ws_host = torch.empty(max(256, pa.pa_store_decode_host_workspace_size(
+        c.B, c.Hq, c.Hkv, c.D, c.max_blocks_per_seq, c.block_size)), dtype=torch.uint8, device=dev)
+    h2d = h_total  # the packed span, alignment gaps included
     d2h = h_out.numel() * h_out.element_size()
     e_steps = 0 if args.no_e2e else max(1, min(args.steps, 200))
 
+    host_s = [0.0]
+
     def e2e_step():
-        d_buf.copy_(h_buf, non_blocking=True)
+        q, kn, vn, bt, cl = h_in
+        t = time.perf_counter()
+        pa.pa_store_decode_host(h_out, q, kn, vn, L.kc, L.vc, bt, cl, c.scale, workspace=ws_host)
+        host_s[0] += time.perf_counter() - t
+        stream.synchronize()
+
+    # the same step with torch staging the same packed buffer (one copy) around the device
+    # call, for comparison
+    d_buf = torch.empty(h_total, dtype=torch.uint8, device=dev)
+    d_in = [d_buf[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape)
+            for x, o in zip(h_in, h_offs)]
+
+    def torch_staged_step():
+        d_buf.copy_(h_pack, non_blocking=True)
         q, kn, vn, bt, cl = d_in
-        pa.pa_store_decode(L.out, q, kn, vn, L.kc, L.vc, bt, cl, L.c.scale, workspace=L.ws)
+        pa.pa_store_decode(L.out, q, kn, vn, L.kc, L.vc, bt, cl, c.scale, workspace=L.ws)
         h_out.copy_(L.out, non_blocking=True)
         stream.synchronize()
 
-    for _ in range(3 if e_steps else 0):
-        e2e_step()
-    barrier()
-    torch.cuda.synchronize()
-    e0, e1 = ev(), ev()
-    e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        e_ms = slowest(torch, e_ms, dist, dev)
+    def timed_loop(fn):
+        for _ in range(3 if e_steps else 0):
+            fn()
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        for _ in range(e_steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if dist is not None:
+            ms = slowest(torch, ms, dist, dev)
+        return ms
+
+    e_ms = timed_loop(e2e_step)
+    host_us = host_s[0] / (e_steps + 3) * 1e6 if e_steps else None  # the call itself, on the host
     e2e_value = weak_gbs(ws_, nbytes[0] * e_steps, e_ms) if e_steps else None
+    ts_ms = timed_loop(torch_staged_step) if e_steps else 0.0
+    e2e_torch_staged = weak_gbs(ws_, nbytes[0] * e_steps, ts_ms) if e_steps else None
 
     # ---- other rows: prefill with a cached prefix (store + varlen prefill) ----
     rows = {}
@@ -497,8 +521,13 @@ def run_gpu(args, ws_, rank, local):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e_steps,
-                "note": "pool resident; per step: one H2D copy of q, new K/V, tables, lengths "
-                        "(one pinned buffer); pa_store_decode; D2H of the output; stream sync"},
+                "call": "pa_store_decode_host (C-ABI, host buffers)",
+                "note": "pool resident; per step one call that queues the H2D copy of q, new K/V, "
+                        "tables and lengths (one pinned buffer in the library's packed layout), "
+                        "the fused store + decode, and the D2H copy of the output; then a "
+                        "stream sync",
+                "torch_staged_value": e2e_torch_staged, "host_us_per_call": host_us,
+                "device_ms_per_step": ms_step, "e2e_ms_per_step": e_ms / e_steps if e_steps else None},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "rows": rows,

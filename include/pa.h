@@ -156,6 +156,52 @@ pa_status pa_store_decode(void *out, const void *q, const void *k_new, const voi
                           cudaStream_t stream);
 
 /*
+ * pa_store_decode_host: pa_store_decode for a step whose inputs and output live in host memory
+ * (the pools stay on the device, as in an engine). On `stream`, in order: one copy host -> device
+ * of each input (q, k_new, v_new, block_tables, context_lens) into the device workspace, the
+ * store + decode launches, and one copy device -> host of the output. The call returns once these
+ * are queued; the host buffers must stay valid and unchanged until the stream has passed them
+ * (synchronise the stream before reading out_host). Page-locked host memory lets the copies run
+ * asynchronously; pageable memory works too, with copies that block.
+ *
+ * Source: as pa_store_decode ("nano-vLLM Part 4" section 3: the engine moves each step's inputs
+ * to the device and reads the sampled result back).
+ *
+ * out_host, q_host               [B, Hq, D] (fp16/bf16 bits), host
+ * k_new_host, v_new_host         [B, Hkv, D], host
+ * block_tables_host              int32 [B, max_blocks_per_seq], host
+ * context_lens_host              int32 [B], host
+ * k_cache, v_cache               device pools, as pa_store_decode
+ * workspace                      device memory of at least pa_store_decode_host_workspace_size()
+ *                                bytes, 256-byte aligned: the staged inputs and output, then
+ *                                pa_decode's workspace
+ * Inputs packed in one host buffer at the offsets pa_store_decode_host_layout() gives (q_host at
+ * offset 0 of the buffer, the others after it) travel in one copy instead of five. When that
+ * buffer (or out_host) is page-locked memory registered with CUDA and mapped into the device's
+ * address space, 16-byte aligned, the copy is done by a kernel whose SMs load (store) the host
+ * bytes directly; otherwise by cudaMemcpyAsync.
+ * Errors: as pa_store_decode; PA_ERR_NULL for a missing host pointer; PA_ERR_WORKSPACE when the
+ * workspace is missing, too small or unaligned; PA_ERR_CUDA when a copy cannot be queued.
+ */
+size_t pa_store_decode_host_workspace_size(int B, int Hq, int Hkv, int D, int max_blocks_per_seq,
+                                           int block_size);
+/*
+ * pa_store_decode_host_layout: the packed host layout of a step's inputs. Writes the byte offsets
+ * of q, k_new, v_new, block_tables and context_lens (in that order, 256-byte aligned, q at 0) to
+ * offsets[0..4] and returns the bytes a buffer holding all five needs; returns 0 (offsets
+ * untouched) for an empty batch or invalid sizes. offsets may be NULL to query the size alone.
+ */
+size_t pa_store_decode_host_layout(int B, int Hq, int Hkv, int D, int max_blocks_per_seq,
+                                   size_t *offsets);
+pa_status pa_store_decode_host(void *out_host, const void *q_host, const void *k_new_host,
+                               const void *v_new_host, void *k_cache, void *v_cache,
+                               const int32_t *block_tables_host, int max_blocks_per_seq,
+                               const int32_t *context_lens_host, int B, int Hq, int Hkv, int D,
+                               int block_size, int num_blocks, float scale, pa_dtype dtype,
+                               void *workspace, size_t workspace_bytes, int32_t *err,
+                               cudaStream_t stream);
+
+/*
  * pa_prefill_varlen: variable-length (causal) prefill attention over packed prompts, with a
  * cached prefix read from the pool.
  *

@@ -18,6 +18,7 @@ LIB_PATH = PKG / "_build" / "libpagedattn.so"
 PA_F16, PA_BF16 = 0, 1
 PA_DEVERR_SLOT, PA_DEVERR_TABLE, PA_DEVERR_LENGTH = 1, 2, 4
 EXPORTS = ("pa_store_kv", "pa_decode_workspace_size", "pa_decode", "pa_store_decode",
+           "pa_store_decode_host", "pa_store_decode_host_workspace_size", "pa_store_decode_host_layout",
            "pa_prefill_varlen", "pa_decode_noalloc", "pa_status_string", "pa_bm_create",
            "pa_bm_destroy", "pa_bm_allocate", "pa_bm_can_allocate", "pa_bm_append",
            "pa_bm_release", "pa_bm_block_table", "pa_bm_num_tokens", "pa_bm_num_free",
@@ -51,6 +52,12 @@ def load(path: Path | str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_decode.restype = I
     lib.pa_store_decode.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, P, Z, P, P]
     lib.pa_store_decode.restype = I
+    lib.pa_store_decode_host.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, P, Z, P, P]
+    lib.pa_store_decode_host.restype = I
+    lib.pa_store_decode_host_workspace_size.argtypes = [I, I, I, I, I, I]
+    lib.pa_store_decode_host_workspace_size.restype = Z
+    lib.pa_store_decode_host_layout.argtypes = [I, I, I, I, I, P]
+    lib.pa_store_decode_host_layout.restype = Z
     lib.pa_prefill_varlen.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, I, I, I, I, I, I,
                                       F, I, I, P, P]
     lib.pa_prefill_varlen.restype = I
@@ -184,6 +191,53 @@ def pa_store_decode(out, q, k_new, v_new, k_cache, v_cache, block_tables, contex
         _i32(block_tables, "block_tables"), maxb, _i32(context_lens, "context_lens"), B, Hq, Hkv,
         D, bs, NB, float(scale), dt, _ptr(workspace), ws_bytes, _i32(err, "err"),
         _stream(stream, q)))
+
+
+def _hptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("host tensors expected (page-locked ones let the copies run asynchronously)")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def pa_store_decode_host_workspace_size(B, Hq, Hkv, D, max_blocks_per_seq, block_size) -> int:
+    return int(load().pa_store_decode_host_workspace_size(B, Hq, Hkv, D, max_blocks_per_seq, block_size))
+
+
+def pa_store_decode_host_layout(B, Hq, Hkv, D, max_blocks_per_seq):
+    """(offsets of q, k_new, v_new, block_tables, context_lens; total bytes) of the packed host
+    layout whose inputs pa_store_decode_host moves in one copy; (None, 0) for invalid sizes."""
+    offs = (ctypes.c_size_t * 5)()
+    n = int(load().pa_store_decode_host_layout(B, Hq, Hkv, D, max_blocks_per_seq, offs))
+    return (tuple(int(x) for x in offs) if n else None), n
+
+
+def pa_store_decode_host(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                         scale: float, workspace, err=None, stream=None) -> None:
+    """pa_store_decode with q, k_new, v_new, block_tables, context_lens and out in host memory
+    (the pools on the device): the library copies the inputs in, runs the step and copies the
+    output back, all queued on the stream. Synchronise the stream before reading `out`."""
+    NB, bs, Hkv, D = k_cache.shape
+    B, Hq, Dq = q.shape
+    if (Dq != D or tuple(out.shape) != (B, Hq, D) or tuple(k_new.shape) != (B, Hkv, D) or
+            tuple(v_new.shape) != (B, Hkv, D) or block_tables.shape[0] != B or
+            context_lens.shape != (B,)):
+        raise ValueError("shape mismatch")
+    dt = _dtype(q)
+    if any(t.dtype != q.dtype for t in (out, k_new, v_new, k_cache, v_cache)):
+        raise TypeError("q, out, the new rows and the pools must share a dtype")
+    for name, t in (("block_tables", block_tables), ("context_lens", context_lens)):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{name} must be int32")
+    maxb = block_tables.shape[1]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("pa_store_decode_host", load().pa_store_decode_host(
+        _hptr(out), _hptr(q), _hptr(k_new), _hptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _hptr(block_tables), maxb, _hptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale), dt,
+        _ptr(workspace), ws_bytes, _i32(err, "err"), _stream(stream, k_cache)))
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,

@@ -11,6 +11,18 @@ namespace pa {
 int device_sm_count();  // SMs of the current device (cached per device)
 
 // ------------------------------------------------------------------------------------------
+// Staging between host memory and the device by the SMs (stage.cu).
+// The device address of the host range [p, p + bytes) when the device may load and store it
+// directly: page-locked memory registered with CUDA whose first and last bytes map to device
+// addresses bytes - 1 apart. nullptr otherwise (pageable or other memory, a range that leaves its
+// allocation, no CUDA device).
+void *mapped_host(const void *p, size_t bytes);
+// Copies bytes (a multiple of 4; both addresses 16-byte aligned) with a kernel on `stream`;
+// dependent: launched as a programmatic dependent of the previous grid (which must let it launch
+// early and complete before this one reads).
+cudaError_t launch_stage(void *dst, const void *src, size_t bytes, bool dependent, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
 struct StoreArgs {
     const void *k, *v;
     void *k_cache, *v_cache;

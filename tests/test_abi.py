@@ -136,3 +136,50 @@ def test_store_decode_host_checks(lib):
     need = lib.pa_decode_workspace_size(2, 4, 2, 64, 4, 16)
     if need:
         assert _store_decode(lib, ws=None, wsb=0) == 5
+
+
+def _store_decode_host(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, kn=FAKE, vn=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, maxb=4, cl=FAKE, B=2,
+             Hq=4, Hkv=2, D=64, bs=16, nb=8, scale=0.125, dt=0, ws=None, wsb=0, err=None, stream=None)
+    a.update(kw)
+    return lib.pa_store_decode_host(*a.values())
+
+
+def test_store_decode_host_entry_checks(lib):
+    # every case below returns before the first copy is queued
+    assert _store_decode_host(lib, dt=2) == 3
+    assert _store_decode_host(lib, Hq=5) == 2
+    assert _store_decode_host(lib, D=96) == 4
+    assert _store_decode_host(lib, bs=0) == 2
+    assert _store_decode_host(lib, B=0) == 0          # empty batch: no-op, nothing copied
+    assert _store_decode_host(lib, q=None) == 1
+    assert _store_decode_host(lib, out=None) == 1
+    assert _store_decode_host(lib, kc=None) == 1
+    assert _store_decode_host(lib, bt=None) == 1      # a table width without a table
+    assert _store_decode_host(lib, ws=None, wsb=0) == 5
+    need = lib.pa_store_decode_host_workspace_size(2, 4, 2, 64, 4, 16)
+    assert _store_decode_host(lib, ws=FAKE, wsb=need - 1) == 5
+    assert _store_decode_host(lib, ws=FAKE + 128, wsb=need) == 5   # staged regions need 256-byte alignment
+
+
+def test_store_decode_host_workspace_covers_staging(lib):
+    B, Hq, Hkv, D, maxb, bs = 3, 8, 2, 128, 5, 16
+    need = lib.pa_store_decode_host_workspace_size(B, Hq, Hkv, D, maxb, bs)
+    staged = B * Hq * D * 2 * 2 + B * Hkv * D * 2 * 2 + B * maxb * 4 + B * 4
+    assert need >= staged + lib.pa_decode_workspace_size(B, Hq, Hkv, D, maxb, bs)
+    assert need % 256 == 0
+    assert lib.pa_store_decode_host_workspace_size(0, Hq, Hkv, D, maxb, bs) == 0
+    assert lib.pa_store_decode_host_workspace_size(B, 5, Hkv, D, maxb, bs) == 0
+
+
+def test_store_decode_host_layout(lib):
+    B, Hq, Hkv, D, maxb = 5, 16, 8, 128, 7
+    offs, n = binding.pa_store_decode_host_layout(B, Hq, Hkv, D, maxb)
+    sizes = [B * Hq * D * 2, B * Hkv * D * 2, B * Hkv * D * 2, B * maxb * 4, B * 4]
+    assert offs[0] == 0 and all(o % 256 == 0 for o in offs)
+    for i in range(4):  # in order, each region clear of the next
+        assert offs[i] + sizes[i] <= offs[i + 1]
+    assert n == offs[4] + sizes[4]
+    assert lib.pa_store_decode_host_layout(B, Hq, Hkv, D, maxb, None) == n
+    assert binding.pa_store_decode_host_layout(0, Hq, Hkv, D, maxb) == (None, 0)
+    assert binding.pa_store_decode_host_layout(B, 5, Hkv, D, maxb) == (None, 0)
