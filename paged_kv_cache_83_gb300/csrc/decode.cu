@@ -1020,19 +1020,21 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
 }
 
 // One CTA per decode CTA: if that CTA's first pair began in an earlier CTA and ends in this one,
-// combine the pair's partial segments into the output. Every global read that the result depends
-// on is issued in parallel (records, then the segments' max and sum, then the partial rows), so the
-// kernel costs a few memory round trips whatever the number of segments.
+// combine the pair's partial segments into the output. The decode CTAs' tile ranges are the
+// closed-form equal shares of the launch's tiles, so the list of contributing CTAs (and which of
+// each one's two partial slots holds the pair) follows from this CTA's own record with no further
+// reads. After that record, every global read the result depends on (each segment's max, sum and
+// partial row) is issued together, so the kernel costs two memory round trips for up to
+// kMergeChunk segments.
 constexpr int kMergeMaxCtas = 512;  // decode CTAs per launch (2 per SM at most)
+constexpr int kMergeThreads = 256;
 
 template <int D, int G, class E>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const __grid_constant__ DecodeParams p) {
     using T = typename E::T;
-    __shared__ int seg_cta[kMergeMaxCtas];            // contributing CTAs, in CTA order
-    __shared__ unsigned char seg_slot[kMergeMaxCtas];  // which of the CTA's two partials
-    __shared__ float seg_m[kMergeMaxCtas][G];          // segment max (log2 domain), then weight
-    __shared__ float seg_l[kMergeMaxCtas][G];          // segment sum
-    __shared__ float norm[G];
+    constexpr int kOut = (G * D + kMergeThreads - 1) / kMergeThreads;  // outputs per thread
+    constexpr int kMergeChunk = kOut <= 2 ? 8 : 4;                     // segments loaded at once
+    __shared__ int seg_part[kMergeMaxCtas];  // contributing segments: partial slot index, in CTA order
     __shared__ int nseg_s;
     const int c = blockIdx.x, P = gridDim.x, tid = threadIdx.x, lane = tid & 31;
     // what follows in the stream may launch now (it waits for this grid before reading)
@@ -1042,65 +1044,85 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const SegRecord rc = p.rec[c];
     if (rc.b < 0 || rc.pair_start >= rc.lo || rc.pair_start + rc.ntiles > rc.hi) return;
+    const long long x = rc.pair_start, total = rc.total;
+    // decode CTA c' holds tiles [total c' / P, total (c' + 1) / P)
+    auto lo_of = [&](int cc) { return total * cc / P; };
     // first CTA whose range holds the pair's first tile: max{c' : lo(c') <= pair_start}
-    const long long x = rc.pair_start;
-    int c0 = static_cast<int>(((x + 1) * P + rc.total - 1) / rc.total) - 1;
+    int c0 = static_cast<int>(((x + 1) * P + total - 1) / total) - 1;
     if (c0 < 0) c0 = 0;
     if (tid < 32) {  // the CTAs in [c0, c] that hold tiles (ranges can be empty when tiles < CTAs)
         int n = 0;
         for (int base = c0; base <= c; base += 32) {
             const int cc = base + lane;
-            bool has = false;
-            int slot = 0;
-            if (cc <= c) {
-                const SegRecord r = p.rec[cc];
-                has = r.lo < r.hi;
-                slot = (cc == c0 && r.lo < x) ? 1 : 0;
-            }
+            const long long lo = cc <= c ? lo_of(cc) : 0;
+            const bool has = cc <= c && lo < lo_of(cc + 1);
+            // the pair is the last segment of CTA c0 when that CTA began in an earlier pair (slot
+            // 1), and the first segment of every later CTA (slot 0)
+            const int slot = (cc == c0 && lo < x) ? 1 : 0;
             const unsigned m = __ballot_sync(kFull, has);
-            if (has) {
-                const int pos = n + __popc(m & ((1u << lane) - 1u));
-                seg_cta[pos] = cc;
-                seg_slot[pos] = static_cast<unsigned char>(slot);
-            }
+            if (has) seg_part[n + __popc(m & ((1u << lane) - 1u))] = 2 * cc + slot;
             n += __popc(m);
         }
         if (lane == 0) nseg_s = n;
     }
     __syncthreads();
     const int nseg = nseg_s;
-    auto partial = [&](int k, int h) {
-        return p.part + ((static_cast<size_t>(seg_cta[k]) * 2 + seg_slot[k]) * G + h) * (D + 2);
-    };
-    for (int i = tid; i < nseg * G; i += blockDim.x) {
-        const int k = i / G, h = i % G;
-        const float *pp = partial(k, h);
-        seg_m[k][h] = pp[D];
-        seg_l[k][h] = pp[D + 1];
+    int hh[kOut], dd[kOut];
+    float M[kOut], L[kOut], O[kOut];
+#pragma unroll
+    for (int j = 0; j < kOut; ++j) {
+        const int idx = tid + j * kMergeThreads;
+        hh[j] = idx < G * D ? idx / D : -1;
+        dd[j] = idx % D;
+        M[j] = -INFINITY;
+        L[j] = 0.f;
+        O[j] = 0.f;
     }
-    __syncthreads();
-    if (tid < G) {  // reference max, segment weights and the normaliser, segments in order
-        const int h = tid;
-        float M = -INFINITY;
-        for (int k = 0; k < nseg; ++k) M = fmaxf(M, seg_m[k][h]);
-        const float mu = M == -INFINITY ? 0.f : M;
-        float L = 0.f;
-        for (int k = 0; k < nseg; ++k) {
-            const float w = seg_l[k][h] * fast_exp2(seg_m[k][h] - mu);
-            seg_m[k][h] = w;
-            L += w;
+    for (int k0 = 0; k0 < nseg; k0 += kMergeChunk) {
+        float mv[kOut][kMergeChunk], lv[kOut][kMergeChunk], ov[kOut][kMergeChunk];
+#pragma unroll
+        for (int k = 0; k < kMergeChunk; ++k) {
+            const bool in = k0 + k < nseg;
+            const float *seg = in ? p.part + static_cast<size_t>(seg_part[k0 + k]) * G * (D + 2) : nullptr;
+#pragma unroll
+            for (int j = 0; j < kOut; ++j) {
+                if (in && hh[j] >= 0) {
+                    const float *row = seg + hh[j] * (D + 2);
+                    mv[j][k] = row[D];
+                    lv[j][k] = row[D + 1];
+                    ov[j][k] = row[dd[j]];
+                } else {
+                    mv[j][k] = -INFINITY;
+                    lv[j][k] = 0.f;
+                    ov[j][k] = 0.f;
+                }
+            }
         }
-        norm[h] = L;
+#pragma unroll
+        for (int j = 0; j < kOut; ++j) {
+            // the running (max, sum, weighted row) of the segments so far, rescaled to the new max
+            float cm = M[j];
+#pragma unroll
+            for (int k = 0; k < kMergeChunk; ++k) cm = fmaxf(cm, mv[j][k]);
+            const float mu = cm == -INFINITY ? 0.f : cm;
+            const float s = M[j] == -INFINITY ? 0.f : fast_exp2(M[j] - mu);
+            float l = L[j] * s, o = O[j] * s;
+#pragma unroll
+            for (int k = 0; k < kMergeChunk; ++k) {
+                const float w = mv[j][k] == -INFINITY ? 0.f : lv[j][k] * fast_exp2(mv[j][k] - mu);
+                l += w;
+                o = fmaf(w, ov[j][k], o);
+            }
+            M[j] = cm;
+            L[j] = l;
+            O[j] = o;
+        }
     }
-    __syncthreads();
     const size_t bh = static_cast<size_t>(rc.b) * p.Hq + static_cast<size_t>(rc.g) * G;
-    for (int idx = tid; idx < G * D; idx += blockDim.x) {
-        const int h = idx / D, d = idx % D;
-        float O = 0.f;
-        for (int k = 0; k < nseg; ++k) O = fmaf(seg_m[k][h], partial(k, h)[d], O);
-        const float L = norm[h];
-        static_cast<T *>(p.out)[(bh + h) * D + d] = T(L > 0.f ? O / L : 0.f);
-    }
+#pragma unroll
+    for (int j = 0; j < kOut; ++j)
+        if (hh[j] >= 0)
+            static_cast<T *>(p.out)[(bh + hh[j]) * D + dd[j]] = T(L[j] > 0.f ? O[j] / L[j] : 0.f);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1215,7 +1237,7 @@ cudaError_t launch_typed(DecodeParams &prm, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(P);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cfg.attrs = attr;
