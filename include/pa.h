@@ -91,11 +91,13 @@ pa_status pa_store_kv(const void *k, const void *v, void *k_cache, void *v_cache
 
 /*
  * pa_decode_workspace_size: bytes of scratch pa_decode needs for these sizes on the current
- * device: for each SM, two partial results (G query heads x (D + 2) fp32: output, running max,
- * sum) of the at most two context pieces it shares with a neighbour, plus a 48-byte record. It
- * depends only on the group size G = Hq / Hkv, D and the SM count (about 1.3 MB at most on a
- * GB300), not on the batch or the context lengths. Never fails; returns 0 for sizes that
- * pa_decode would reject.
+ * device. The work is cut into units (one per CTA, one or two CTAs per SM; for group sizes up to
+ * 3 and batches of at most 288 sequences, four more per CTA that CTAs take as they finish); each
+ * unit has two partial results (G query heads x (D + 2) fp32: output, running max, sum) for the
+ * at most two context pieces it shares with a neighbour, plus a 64-byte record, and the launch a
+ * 16-byte counter. It depends on the group size G = Hq / Hkv, D, whether the batch fits one CTA's
+ * threads and the SM count (about 4.9 MB at most on a GB300), not on the context lengths. Never
+ * fails; returns 0 for sizes that pa_decode would reject.
  */
 size_t pa_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_blocks_per_seq,
                                 int block_size);
@@ -255,8 +257,10 @@ pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void 
  * which every GPU that loads this library holds until the process exits. The call itself
  * allocates nothing (no cudaMalloc, no cudaFree, no allocating library routine).
  *
- * - Limit: sizes whose pa_decode_workspace_size() exceeds PA_DECODE_NOALLOC_SCRATCH_BYTES are
- *   rejected with PA_ERR_WORKSPACE before anything is launched (use pa_decode for them).
+ * - Limit: it always cuts the work into one unit per CTA (no units taken as CTAs finish), so it
+ *   needs the partials of those units only; sizes for which they exceed
+ *   PA_DECODE_NOALLOC_SCRATCH_BYTES (GQA groups of 8 at D = 128, for instance) are rejected with
+ *   PA_ERR_WORKSPACE before anything is launched (use pa_decode for them).
  * - Set-up: the first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call before any stream
  *   capture. A failed lookup returns PA_ERR_CUDA.

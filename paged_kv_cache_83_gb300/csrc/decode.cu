@@ -39,6 +39,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "pa_internal.h"
 
 namespace pa {
@@ -57,7 +59,7 @@ constexpr int kIdRing = 4;                   // each producer's ring of prepared
 static_assert(kIdRing > kLook && (kIdRing & (kIdRing - 1)) == 0, "block-id ring");
 
 struct PrepTile {
-    int b, g, t, n, nt, pad[3];
+    int b, g, t, n, nt, unit, flags, pad;  // b < 0: no tile (the CTA's work is done)
 };
 // tensor-core consumers from this group size on
 constexpr int kMmaMinGroup = 4;
@@ -80,20 +82,35 @@ __host__ __device__ constexpr int threads_for(int D, int G) { return 32 * (produ
 constexpr int kFirst = 1;  // first tile of a segment: reset the state, read q
 constexpr int kLast = 2;   // last tile of a segment: combine the warps and write
 constexpr int kWhole = 4;  // the segment is its pair's whole context: write the output
-constexpr int kSlot1 = 8;  // partial segment that is not the CTA's first: workspace slot 1
+constexpr int kSlot1 = 8;  // partial segment that is not the unit's first: workspace slot 1
+constexpr int kEnd = 16;   // no tile: the CTA's work is done (dynamic tail)
+
+// Dynamic tail (one producer warp, batches of at most one CTA's threads). The launch's tiles
+// [0, F) are cut into one equal contiguous unit per CTA, as in the static scheme; the last
+// 1/kTailDiv of them, [F, total), into kTailUnitsPerCta units per CTA that CTAs take from a
+// counter as they finish, so that CTAs on slower SMs take fewer of them. All unit bounds are
+// closed-form, so the merge finds the pieces of a pair without a list.
+constexpr int kTailDiv = 8;
+constexpr int kTailUnitsPerCta = 4;
+constexpr int kDynMinTilesPerCta = 64;  // smaller launches keep the static scheme
 
 struct TileMeta {
     int b, g, flags, all_valid;  // all_valid: every one of the 128 rows is a context position
     unsigned long long valid[2];  // bit r of the 128-bit mask: tile row r is a context position
-    int newrow, pad;              // row whose K/V are in the spare row (a new token), or -1
+    int newrow, unit;             // row whose K/V are in the spare row (a new token), or -1;
+                                  // the unit the tile belongs to
 };
 
-// What the merge kernel needs to know about one CTA.
+// What the merge kernel needs to know about one unit of work (a CTA's static range, or one
+// unit of the dynamic tail).
 struct SegRecord {
-    long long lo, hi;        // the CTA's tile range
-    long long pair_start;    // global index of the first tile of the CTA's first pair
+    long long lo, hi;        // the unit's tile range
+    long long pair_start;    // global index of the first tile of the unit's first pair
     long long total;         // tiles in the whole launch
-    int b, g, ntiles, pad;   // that pair and its tile count; b < 0: empty range
+    long long F;             // tiles in the static units (total without a dynamic tail)
+    int b, g, ntiles;        // that pair and its tile count; b < 0: empty range
+    int P, K2;               // static units (= CTAs) and tail units of the launch
+    unsigned epoch;          // the launch that wrote the record
 };
 
 struct DecodeParams {
@@ -103,10 +120,13 @@ struct DecodeParams {
     void *k_cache, *v_cache;    // the pools (written by the fused store only)
     const int32_t *block_tables, *context_lens;
     void *out;
-    float *part;     // [P][2][G][D + 2]: normalised O, max (log2 units), sum
-    SegRecord *rec;  // [P]
+    float *part;     // [units][2][G][D + 2]: normalised O, max (log2 units), sum
+    SegRecord *rec;  // [units]
+    unsigned long long *ctr;  // dynamic tail: [0] epoch tag, [1] tickets handed out (low word)
     int32_t *err;
     int B, Hq, Hkv, max_blocks, num_blocks, box_rows, stages;
+    int tail_units;  // units of the dynamic tail the workspace holds (0: static scheme only)
+    unsigned epoch;  // distinct for every launch (never 0)
     BlockGeom geom;
     float scale_log2;
 };
@@ -162,12 +182,18 @@ struct Shape {
     }
 };
 
+// the dynamic tail's per-sequence tile offsets (int32, batches of at most one CTA's threads)
+__host__ __device__ constexpr int dyn_seq_bytes(int D, int G) {
+    return producers_for(D, G) == 1 ? (threads_for(D, G) + 1 + 1) / 2 * 8 : 0;
+}
+
 template <int D, int G, int CPS>
 constexpr int fixed_smem() {
     // + metas, barriers, scan scratch (1 KB), the slack that aligns the ring (1 KB) and the
     // producer's ring of prepared tiles
     using S = Shape<D, G, CPS>;
-    return S::RED_BYTES + S::SCRATCH_BYTES + 2048 + producers_for(D, G) * kIdRing * (S::TN * 4 + 32);
+    return S::RED_BYTES + S::SCRATCH_BYTES + 2048 + producers_for(D, G) * kIdRing * (S::TN * 4 + 32) +
+           dyn_seq_bytes(D, G);
 }
 
 // All 32 lanes wait for the phase, then the warp reconverges; false (for every lane) if the wait
@@ -229,6 +255,41 @@ __device__ __forceinline__ void mma_k8(float (&d)[4], uint32_t a0, uint32_t a1, 
 }
 
 // stages of TN positions over sequence b's context
+// The next ticket of this launch from the dynamic tail's counter: 0, 1, 2, ... in the order CTAs
+// ask, one atomic add each. The counter is reset once per launch, by whichever CTA asks first: the
+// tag word holds the epoch of the launch the counter belongs to (with bit 32 set while a CTA is
+// resetting it), so a word another launch left, or one never written, is reset before use and the
+// workspace needs no clearing between launches. `ready` (per CTA) remembers that this launch's
+// reset has been seen. -1 if the wait for another CTA's reset ran out.
+__device__ __forceinline__ long long take_ticket(unsigned long long *tag, unsigned *cnt, unsigned epoch,
+                                                 bool &ready) {
+    if (!ready) {
+        const unsigned long long mine = epoch, resetting = (1ull << 32) | epoch;
+        unsigned long long t = *reinterpret_cast<volatile unsigned long long *>(tag);
+        const uint64_t t0 = globaltimer_ns();
+        for (int it = 0;; ++it) {
+            if (t == mine) break;
+            if (t != resetting) {
+                const unsigned long long prev = atomicCAS(tag, t, resetting);
+                if (prev == t) {  // this CTA resets the counter
+                    atomicExch(cnt, 0u);
+                    __threadfence();
+                    atomicExch(tag, mine);
+                    break;
+                }
+                t = prev;
+                continue;
+            }
+            if ((it & 15) == 15 && globaltimer_ns() - t0 > kWaitLimitNs) return -1;
+            __nanosleep(64);
+            t = *reinterpret_cast<volatile unsigned long long *>(tag);
+        }
+        __threadfence();
+        ready = true;
+    }
+    return static_cast<long long>(atomicAdd(cnt, 1u));
+}
+
 template <int TN>
 __device__ __forceinline__ int ntiles_of(const DecodeParams &p, int b, long long cap) {
     const int n = p.context_lens[b];
@@ -269,6 +330,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
     volatile int *abort_flag = reinterpret_cast<volatile int *>(scan + 20);
     PrepTile *prep = reinterpret_cast<PrepTile *>(scan + 24);  // [producers][kIdRing]
     int *idring = reinterpret_cast<int *>(prep + kProducers * kIdRing);  // [producers][kIdRing][TN]
+    int *seqpre = idring + kProducers * kIdRing * S::TN;  // dynamic tail: first tile of each sequence
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = gridDim.x, cta = blockIdx.x;
@@ -331,6 +393,12 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
             scan[16] = tid;
             scan[17] = excl;
         }
+        if constexpr (dyn_seq_bytes(D, G) > 0) {
+            if (total < (1ll << 31)) {  // the only case the dynamic tail runs in
+                if (tid < p.B) seqpre[tid] = static_cast<int>(excl);
+                if (tid == 0) seqpre[p.B] = static_cast<int>(total);
+            }
+        }
         __syncthreads();
     } else {
         // ---- pass 1: tiles per sequence, the total ----
@@ -375,24 +443,48 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
     const int b0 = static_cast<int>(scan[16]);
     const long long seq_start = scan[17];  // global index of tile (b0, 0, 0)
 
-    if (tid == 0) {
-        SegRecord r{};
-        r.lo = lo;
-        r.hi = hi;
-        r.total = total;
-        r.b = -1;
-        if (lo < hi && b0 >= 0) {
-            const int nt = ntiles_of<S::TN>(p, b0, cap);
-            const long long off = lo - seq_start;
-            r.b = b0;
-            r.g = static_cast<int>(off / nt);
-            r.ntiles = nt;
-            r.pair_start = seq_start + static_cast<long long>(r.g) * nt;
+    // the dynamic tail runs for large enough batches of at most one CTA's threads (its offsets
+    // per sequence live in shared memory) when the workspace holds its units; the choice is the
+    // same in every CTA
+    bool dyn = false;
+    long long F = total;
+    int K2 = 0;
+    if constexpr (dyn_seq_bytes(D, G) > 0) {
+        if (p.tail_units > 0 && p.B <= kThreads && total < (1ll << 31) &&
+            total >= static_cast<long long>(kDynMinTilesPerCta) * P) {
+            dyn = true;
+            K2 = p.tail_units;
+            F = total - total / kTailDiv;
         }
-        p.rec[cta] = r;
     }
-    if (lo >= hi || b0 < 0) return;
-    const long long count = hi - lo;
+    auto make_rec = [&](long long ulo, long long uhi) {
+        SegRecord r{};
+        r.lo = ulo;
+        r.hi = uhi;
+        r.total = total;
+        r.F = F;
+        r.P = P;
+        r.K2 = K2;
+        r.epoch = p.epoch;
+        r.b = -1;
+        return r;
+    };
+    if (!dyn) {
+        if (tid == 0) {
+            SegRecord r = make_rec(lo, hi);
+            if (lo < hi && b0 >= 0) {
+                const int nt = ntiles_of<S::TN>(p, b0, cap);
+                const long long off = lo - seq_start;
+                r.b = b0;
+                r.g = static_cast<int>(off / nt);
+                r.ntiles = nt;
+                r.pair_start = seq_start + static_cast<long long>(r.g) * nt;
+            }
+            p.rec[cta] = r;
+        }
+        if (lo >= hi || b0 < 0) return;
+    }
+    const long long count = hi - lo;  // static scheme: the CTA's tiles
 
     if (warp < kProducers) {
         // ======================= producers =======================
@@ -407,15 +499,24 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
         const int R = p.box_rows, nbox = TN / R;
         const uint32_t box_bytes = static_cast<uint32_t>(R) * D * 2;
         const unsigned long long box_rows_mask = R == 64 ? ~0ull : ((1ull << R) - 1ull);
-        // walker: the next tile to prepare
-        int b = b0;
-        int nt = ntiles_of<S::TN>(p, b, cap);
-        int n = p.context_lens[b];
-        const long long off = lo - seq_start;
-        int g = static_cast<int>(off / nt), t = static_cast<int>(off % nt);
-        // the CTA's first segment: tiles [0, first_len); it began inside its pair if t > 0
-        const long long first_len = min(count, static_cast<long long>(nt - t));
-        const bool first_mid = t > 0;
+        // The unit being walked: `u_count` tiles from tile u_lo of the launch; the walker
+        // (b, g, t) is the next tile to prepare, `u_pos` its index in the unit. The unit's first
+        // segment is its tiles [0, first_len); it began inside its pair if first_mid.
+        long long unit = cta, u_count = 0, u_pos = 0, first_len = 0;
+        bool first_mid = false, done = false, took_static = false, ticket_ready = false;
+        int b = 0, nt = 1, n = 0, g = 0, t = 0;
+        auto seed = [&](int sb, long long sstart, long long X, long long cnt) {
+            b = sb;
+            nt = ntiles_of<S::TN>(p, b, cap);
+            n = p.context_lens[b];
+            const long long off = X - sstart;
+            g = static_cast<int>(off / nt);
+            t = static_cast<int>(off % nt);
+            u_count = cnt;
+            u_pos = 0;
+            first_len = min(cnt, static_cast<long long>(nt - t));
+            first_mid = t > 0;
+        };
         auto advance = [&]() {
             if (++t == nt) {
                 t = 0;
@@ -428,16 +529,90 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                 }
             }
         };
-        for (int k = 0; k < pw && k < count; ++k) advance();
+        // dynamic tail: bounds of unit v (static units first, then the tail's)
+        auto unit_lo = [&](long long v) -> long long {
+            return v <= P ? F * v / P : F + (total - F) * (v - P) / K2;
+        };
+        // dynamic tail: the sequence holding tile X (offsets are non-decreasing, seqpre[B] = total)
+        auto find_seq = [&](long long X) -> int {
+            int l = 0, h = p.B;
+            while (h - l > 1) {
+                const int mid = (l + h) >> 1;
+                if (seqpre[mid] <= X) l = mid;
+                else h = mid;
+            }
+            return l;
+        };
+        // dynamic tail: move the walker to the next unit that holds tiles (first the CTA's static
+        // one, then tickets); records every unit taken, empty ones included. Warp-uniform.
+        auto next_unit = [&]() {
+            for (;;) {
+                long long v;
+                if (!took_static) {
+                    took_static = true;
+                    v = cta;
+                } else {
+                    long long tk = 0;
+                    if (lane == 0)
+                        tk = take_ticket(p.ctr, reinterpret_cast<unsigned *>(p.ctr + 1), p.epoch, ticket_ready);
+                    tk = __shfl_sync(kFull, tk, 0);
+                    if (tk < 0) {
+                        if (lane == 0) {
+                            raise_err(p.err, PA_DEVERR_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                        done = true;
+                        return;
+                    }
+                    if (tk >= K2) {
+                        done = true;
+                        return;
+                    }
+                    v = P + tk;
+                }
+                const long long vlo = unit_lo(v), vhi = unit_lo(v + 1);
+                SegRecord r = make_rec(vlo, vhi);
+                if (vlo < vhi) {
+                    const int sb = find_seq(vlo);
+                    seed(sb, seqpre[sb], vlo, vhi - vlo);
+                    unit = v;
+                    r.b = b;
+                    r.g = g;
+                    r.ntiles = nt;
+                    r.pair_start = seqpre[sb] + static_cast<long long>(g) * nt;
+                }
+                if (lane == 0) p.rec[v] = r;
+                if (vlo < vhi) return;
+            }
+        };
+        if (!dyn) {
+            seed(b0, seq_start, lo, count);
+            for (int k = 0; k < pw && k < count; ++k) advance();
+            u_pos = pw;
+        }
         PrepTile *myprep = prep + pw * kIdRing;
         int *myids = idring + pw * kIdRing * TN;
         // Each producer prepares its tiles kLook of its own steps ahead of the one it issues:
-        // preparing records the tile's coordinates and queues cp.async copies of its block ids
-        // (lane l: boxes l and l + 32) into a ring in shared memory, so the block-table reads are
-        // in flight while earlier tiles are issued. Every step commits one cp.async group per lane.
+        // preparing records the tile's coordinates and flags and queues cp.async copies of its
+        // block ids (lane l: boxes l and l + 32) into a ring in shared memory, so the block-table
+        // reads are in flight while earlier tiles are issued. Every step commits one cp.async
+        // group per lane. With the dynamic tail a step past the CTA's last tile records "no tile".
         auto prepare = [&](long long j) {
             const int sl = static_cast<int>(j % kIdRing);
-            if (lane == 0) myprep[sl] = PrepTile{b, g, t, n, nt};
+            if (dyn && !done && u_pos == u_count) next_unit();
+            if (done) {
+                if (lane == 0) myprep[sl].b = -1;
+                cp_async_commit();
+                return;
+            }
+            const bool first = u_pos == 0 || t == 0;
+            const bool last = u_pos == u_count - 1 || t == nt - 1;
+            const bool in_first = u_pos < first_len;
+            int flags = (first ? kFirst : 0) | (last ? kLast : 0);
+            // the segment covers its whole pair: it ends the pair and began at the pair's start
+            if (last && t == nt - 1 && !(in_first && first_mid)) flags |= kWhole;
+            if (!in_first) flags |= kSlot1;
+            if (lane == 0) myprep[sl] = PrepTile{b, g, t, n, nt, static_cast<int>(unit), flags, 0};
             const int pos0 = t * TN;
             const int nvalid = min(TN, n - pos0);
 #pragma unroll
@@ -448,18 +623,25 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                               p.block_tables + static_cast<size_t>(b) * p.max_blocks + p.geom.block_of(pos0 + k * R));
             }
             cp_async_commit();
+            u_pos += kProducers;
 #pragma unroll
             for (int k = 0; k < kProducers; ++k) advance();
         };
-        const long long my_count = count > pw ? (count - pw + kProducers - 1) / kProducers : 0;
+        const long long my_count =
+            dyn ? (1ll << 62) : (count > pw ? (count - pw + kProducers - 1) / kProducers : 0);
         for (int j = 0; j < kLook; ++j) {
             if (j < my_count) prepare(j);
             else cp_async_commit();
         }
         long long last_i = -1;  // the last tile this producer issued
-        for (long long j = 0; j < my_count; ++j) {
+        long long j = 0;
+        bool aborted = false;
+        for (; j < my_count; ++j) {
             const long long i = pw + static_cast<long long>(kProducers) * j;
-            if (__shfl_sync(kFull, lane == 0 ? *abort_flag : 0, 0)) break;  // warp-uniform
+            if (__shfl_sync(kFull, lane == 0 ? *abort_flag : 0, 0)) {  // warp-uniform
+                aborted = true;
+                break;
+            }
             if (j + kLook < my_count) prepare(j + kLook);
             else cp_async_commit();
             const int stage = static_cast<int>(i % NS);
@@ -469,6 +651,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
             __syncwarp();
             const int sl = static_cast<int>(j % kIdRing);
             const PrepTile pm = myprep[sl];
+            if (pm.b < 0) break;  // dynamic tail: no tiles left
             const int pb_ = pm.b, pg = pm.g, pt = pm.t, pn = pm.n, pnt = pm.nt;
             const int pos0 = pt * TN;
             const int nvalid = min(TN, pn - pos0);
@@ -511,13 +694,8 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                     }
             }
             uint32_t bytes = ngood * 2u * box_bytes;
-            const bool last = (i == count - 1) || (pt == pnt - 1);
-            const bool first = (i == 0) || (pt == 0);
-            const bool in_first = i < first_len;  // the CTA's first segment
-            int flags = (first ? kFirst : 0) | (last ? kLast : 0);
-            // the segment covers its whole pair: it ends the pair and began at the pair's start
-            if (last && pt == pnt - 1 && !(in_first && first_mid)) flags |= kWhole;
-            if (!in_first) flags |= kSlot1;
+            const int flags = pm.flags;
+            const bool first = (flags & kFirst) != 0;
             if (first) bytes += S::Q_BYTES;
             // fused store: the pair's last tile holds the new token (position pn - 1); its rows
             // come from k_new / v_new into the spare rows, not from the pool
@@ -532,6 +710,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                     raise_err(p.err, PA_DEVERR_TIMEOUT);
                     *abort_flag = 1;
                 }
+                aborted = true;
                 break;
             }
             unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
@@ -544,7 +723,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                 m.valid[0] = vm0;
                 m.valid[1] = vm1;
                 m.newrow = new_tok ? (pn - 1) - pos0 : -1;
-                m.pad = 0;
+                m.unit = pm.unit;
                 metas[stage] = m;
                 mbar_arrive_expect_tx(full0 + 8 * stage, bytes);
             }
@@ -621,6 +800,23 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                 }
             }
         }
+        __syncwarp();
+        if (dyn && !aborted) {
+            // tell the consumers there is nothing more: the next stage, with no bytes and the end
+            // flag (after the drain above, whose waits would not see phases this one completes)
+            const long long i = j;
+            const int stage = static_cast<int>(i % NS);
+            const uint32_t phase = static_cast<uint32_t>((i / NS) & 1);
+            if (warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
+                if (lane == 0) {
+                    metas[stage].flags = kEnd;
+                    mbar_arrive(full0 + 8 * stage);
+                }
+            } else if (lane == 0) {
+                raise_err(p.err, PA_DEVERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
         return;
     }
 
@@ -630,7 +826,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
     // Once every consumer warp has put its (max, sum, O) of a finished segment into `red`:
     // combine the 8 warps and write the output (a whole pair) or the CTA's partial. False if
     // a wait ran out.
-    auto combine = [&](int mflags, int mb, int mg) -> bool {
+    auto combine = [&](int mflags, int mb, int mg, int munit) -> bool {
         __syncwarp();
         if (lane == 0) mbar_arrive(cons0);
         bool ok = warp_wait(cons0, seg & 1, abort_flag);
@@ -643,7 +839,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
         }
         const int ct = cw * 32 + lane;
         const size_t bh = static_cast<size_t>(mb) * p.Hq + static_cast<size_t>(mg) * G;
-        float *part = p.part + (static_cast<size_t>(cta) * 2 + ((mflags & kSlot1) ? 1 : 0)) * G * (D + 2);
+        float *part = p.part + (static_cast<size_t>(munit) * 2 + ((mflags & kSlot1) ? 1 : 0)) * G * (D + 2);
         for (int idx = ct; idx < G * D; idx += kConsThreads) {
             const int h = idx / D, d = idx % D;
             float M = -INFINITY;
@@ -702,7 +898,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                 return;
             }
             const TileMeta &m = metas[stage];
-            const int mflags = m.flags, mb = m.b, mg = m.g, mall = m.all_valid, mnew = m.newrow;
+            const int mflags = m.flags, mb = m.b, mg = m.g, mall = m.all_valid, mnew = m.newrow, munit = m.unit;
             const unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
             const uint32_t kb = smem_addr(st), vb = kb + S::TILE_BYTES;
 
@@ -808,7 +1004,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                     }
                 }
             }
-            if (!combine(mflags, mb, mg)) return;
+            if (!combine(mflags, mb, mg, munit)) return;
         }
     } else {
         const int r = lane % S::LPP;
@@ -825,7 +1021,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
         int stage = 0;
         uint32_t phase = 0;
 
-        for (long long i = 0; i < count; ++i) {
+        for (long long i = 0; dyn || i < count; ++i) {
             bool ok = warp_wait(full0 + 8 * stage, phase, abort_flag);
             if (!ok) {
                 if (lane == 0) {
@@ -835,7 +1031,8 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                 return;
             }
             const TileMeta &m = metas[stage];
-            const int mflags = m.flags, mb = m.b, mg = m.g, mall = m.all_valid, mnew = m.newrow;
+            const int mflags = m.flags, mb = m.b, mg = m.g, mall = m.all_valid, mnew = m.newrow, munit = m.unit;
+            if (mflags & kEnd) break;  // dynamic tail: the CTA's work is done
             const unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
             const uint32_t kb = smem_addr(st), vb = kb + S::TILE_BYTES;
             // this warp's rows as a validity mask (bit rl: row rl of the warp)
@@ -1014,59 +1211,53 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                         dst[2 * e + 1] = f2_hi(acc[h][e]);
                     }
                 }
-            if (!combine(mflags, mb, mg)) return;
+            if (!combine(mflags, mb, mg, munit)) return;
         }
     }
 }
 
-// One CTA per decode CTA: if that CTA's first pair began in an earlier CTA and ends in this one,
-// combine the pair's partial segments into the output. The decode CTAs' tile ranges are the
-// closed-form equal shares of the launch's tiles, so the list of contributing CTAs (and which of
-// each one's two partial slots holds the pair) follows from this CTA's own record with no further
-// reads. After that record, every global read the result depends on (each segment's max, sum and
-// partial row) is issued together, so the kernel costs two memory round trips for up to
-// kMergeChunk segments.
+// One CTA per unit of decode work (a decode CTA's static range, or a unit of the dynamic tail): if
+// the unit's first pair began in an earlier unit and ends in this one, combine the pair's partial
+// segments into the output. Unit bounds are closed-form (from the record: the launch's tile count,
+// the static part F, P static units and K2 tail units), so the list of contributing units (and
+// which of each one's two partial slots holds the pair) follows from this unit's own record with
+// no further reads. After that record, every global read the result depends on (each segment's
+// max, sum and partial row) is issued together: two memory round trips for up to kMergeChunk
+// segments. Records another launch left (older epoch) are ignored.
 constexpr int kMergeMaxCtas = 512;  // decode CTAs per launch (2 per SM at most)
 constexpr int kMergeThreads = 256;
+constexpr int kMergeBatch = 512;    // contributing units listed at a time
 
 template <int D, int G, class E>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const __grid_constant__ DecodeParams p) {
     using T = typename E::T;
     constexpr int kOut = (G * D + kMergeThreads - 1) / kMergeThreads;  // outputs per thread
     constexpr int kMergeChunk = kOut <= 2 ? 8 : 4;                     // segments loaded at once
-    __shared__ int seg_part[kMergeMaxCtas];  // contributing segments: partial slot index, in CTA order
+    __shared__ int seg_part[kMergeBatch];  // contributing segments: partial slot index, in unit order
     __shared__ int nseg_s;
-    const int c = blockIdx.x, P = gridDim.x, tid = threadIdx.x, lane = tid & 31;
+    const int c = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
     // what follows in the stream may launch now (it waits for this grid before reading)
     asm volatile("griddepcontrol.launch_dependents;");
     // launched ahead of time (programmatic dependent launch): wait until the decode grid has
     // completed and its writes are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const SegRecord rc = p.rec[c];
-    if (rc.b < 0 || rc.pair_start >= rc.lo || rc.pair_start + rc.ntiles > rc.hi) return;
-    const long long x = rc.pair_start, total = rc.total;
-    // decode CTA c' holds tiles [total c' / P, total (c' + 1) / P)
-    auto lo_of = [&](int cc) { return total * cc / P; };
-    // first CTA whose range holds the pair's first tile: max{c' : lo(c') <= pair_start}
-    int c0 = static_cast<int>(((x + 1) * P + total - 1) / total) - 1;
-    if (c0 < 0) c0 = 0;
-    if (tid < 32) {  // the CTAs in [c0, c] that hold tiles (ranges can be empty when tiles < CTAs)
-        int n = 0;
-        for (int base = c0; base <= c; base += 32) {
-            const int cc = base + lane;
-            const long long lo = cc <= c ? lo_of(cc) : 0;
-            const bool has = cc <= c && lo < lo_of(cc + 1);
-            // the pair is the last segment of CTA c0 when that CTA began in an earlier pair (slot
-            // 1), and the first segment of every later CTA (slot 0)
-            const int slot = (cc == c0 && lo < x) ? 1 : 0;
-            const unsigned m = __ballot_sync(kFull, has);
-            if (has) seg_part[n + __popc(m & ((1u << lane) - 1u))] = 2 * cc + slot;
-            n += __popc(m);
-        }
-        if (lane == 0) nseg_s = n;
-    }
-    __syncthreads();
-    const int nseg = nseg_s;
+    if (rc.epoch != p.epoch || rc.b < 0 || rc.b >= p.B || rc.g < 0 || rc.g >= p.Hkv || rc.P < 1 ||
+        rc.K2 < 0 || (rc.K2 == 0 && c >= rc.P) || rc.total <= 0)
+        return;
+    if (rc.pair_start >= rc.lo || rc.pair_start + rc.ntiles > rc.hi) return;
+    const long long x = rc.pair_start, total = rc.total, F = rc.F;
+    const int P = rc.P, K2 = rc.K2;
+    // unit v holds tiles [lo(v), lo(v + 1))
+    auto lo_of = [&](long long v) -> long long {
+        return v <= P ? F * v / P : F + (total - F) * (v - P) / K2;
+    };
+    // first unit whose range holds the pair's first tile: max{v : lo(v) <= pair_start}, from the
+    // linear piece (static units below F, tail units above) that holds it
+    long long c0l;
+    if (x < F) c0l = ((x + 1) * P + F - 1) / F - 1;
+    else c0l = P + ((x - F + 1) * K2 + (total - F) - 1) / (total - F) - 1;
+    const int c0 = static_cast<int>(c0l < 0 ? 0 : (c0l > c ? c : c0l));
     int hh[kOut], dd[kOut];
     float M[kOut], L[kOut], O[kOut];
 #pragma unroll
@@ -1078,45 +1269,66 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const __gri
         L[j] = 0.f;
         O[j] = 0.f;
     }
-    for (int k0 = 0; k0 < nseg; k0 += kMergeChunk) {
-        float mv[kOut][kMergeChunk], lv[kOut][kMergeChunk], ov[kOut][kMergeChunk];
-#pragma unroll
-        for (int k = 0; k < kMergeChunk; ++k) {
-            const bool in = k0 + k < nseg;
-            const float *seg = in ? p.part + static_cast<size_t>(seg_part[k0 + k]) * G * (D + 2) : nullptr;
-#pragma unroll
-            for (int j = 0; j < kOut; ++j) {
-                if (in && hh[j] >= 0) {
-                    const float *row = seg + hh[j] * (D + 2);
-                    mv[j][k] = row[D];
-                    lv[j][k] = row[D + 1];
-                    ov[j][k] = row[dd[j]];
-                } else {
-                    mv[j][k] = -INFINITY;
-                    lv[j][k] = 0.f;
-                    ov[j][k] = 0.f;
-                }
+    for (int vbase = c0; vbase <= c; vbase += kMergeBatch) {
+        const int vend = min(c, vbase + kMergeBatch - 1);
+        if (tid < 32) {  // the units in [vbase, vend] that hold tiles (a unit can be empty)
+            int n = 0;
+            for (int base = vbase; base <= vend; base += 32) {
+                const int v = base + lane;
+                const long long lo = v <= vend ? lo_of(v) : 0;
+                const bool has = v <= vend && lo < lo_of(v + 1);
+                // the pair is the last segment of unit c0 when that unit began in an earlier pair
+                // (slot 1), and the first segment of every later unit (slot 0)
+                const int slot = (v == c0 && lo < x) ? 1 : 0;
+                const unsigned m = __ballot_sync(kFull, has);
+                if (has) seg_part[n + __popc(m & ((1u << lane) - 1u))] = 2 * v + slot;
+                n += __popc(m);
             }
+            if (lane == 0) nseg_s = n;
         }
-#pragma unroll
-        for (int j = 0; j < kOut; ++j) {
-            // the running (max, sum, weighted row) of the segments so far, rescaled to the new max
-            float cm = M[j];
-#pragma unroll
-            for (int k = 0; k < kMergeChunk; ++k) cm = fmaxf(cm, mv[j][k]);
-            const float mu = cm == -INFINITY ? 0.f : cm;
-            const float s = M[j] == -INFINITY ? 0.f : fast_exp2(M[j] - mu);
-            float l = L[j] * s, o = O[j] * s;
+        __syncthreads();
+        const int nseg = nseg_s;
+        for (int k0 = 0; k0 < nseg; k0 += kMergeChunk) {
+            float mv[kOut][kMergeChunk], lv[kOut][kMergeChunk], ov[kOut][kMergeChunk];
 #pragma unroll
             for (int k = 0; k < kMergeChunk; ++k) {
-                const float w = mv[j][k] == -INFINITY ? 0.f : lv[j][k] * fast_exp2(mv[j][k] - mu);
-                l += w;
-                o = fmaf(w, ov[j][k], o);
+                const bool in = k0 + k < nseg;
+                const float *seg = in ? p.part + static_cast<size_t>(seg_part[k0 + k]) * G * (D + 2) : nullptr;
+#pragma unroll
+                for (int j = 0; j < kOut; ++j) {
+                    if (in && hh[j] >= 0) {
+                        const float *row = seg + hh[j] * (D + 2);
+                        mv[j][k] = row[D];
+                        lv[j][k] = row[D + 1];
+                        ov[j][k] = row[dd[j]];
+                    } else {
+                        mv[j][k] = -INFINITY;
+                        lv[j][k] = 0.f;
+                        ov[j][k] = 0.f;
+                    }
+                }
             }
-            M[j] = cm;
-            L[j] = l;
-            O[j] = o;
+#pragma unroll
+            for (int j = 0; j < kOut; ++j) {
+                // the running (max, sum, weighted row) of the segments so far, rescaled to the new max
+                float cm = M[j];
+#pragma unroll
+                for (int k = 0; k < kMergeChunk; ++k) cm = fmaxf(cm, mv[j][k]);
+                const float mu = cm == -INFINITY ? 0.f : cm;
+                const float s = M[j] == -INFINITY ? 0.f : fast_exp2(M[j] - mu);
+                float l = L[j] * s, o = O[j] * s;
+#pragma unroll
+                for (int k = 0; k < kMergeChunk; ++k) {
+                    const float w = mv[j][k] == -INFINITY ? 0.f : lv[j][k] * fast_exp2(mv[j][k] - mu);
+                    l += w;
+                    o = fmaf(w, ov[j][k], o);
+                }
+                M[j] = cm;
+                L[j] = l;
+                O[j] = o;
+            }
         }
+        __syncthreads();  // seg_part is rebuilt for the next batch
     }
     const size_t bh = static_cast<size_t>(rc.b) * p.Hq + static_cast<size_t>(rc.g) * G;
 #pragma unroll
@@ -1236,7 +1448,7 @@ cudaError_t launch_typed(DecodeParams &prm, cudaStream_t stream) {
     cudaError_t e = cudaLaunchKernelEx(&dcfg, kern, prm);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(P);
+    cfg.gridDim = dim3(P + prm.tail_units);  // one merge CTA per unit
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -1279,6 +1491,40 @@ int launch_ctas_per_sm(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, in
     return stages >= static_cast<long long>(kWideMinStagesPerSm) * device_sm_count() ? 2 : 1;
 }
 
+// Units of the dynamic tail a launch's workspace holds: for the kernels with one producer warp and
+// batches of at most one CTA's threads whose table could hold enough tiles per CTA (an upper
+// bound: every sequence at the table's full length; the kernel decides on the real count); none
+// when the caller's scratch is fixed (allow_dynamic false).
+int tail_units_for(int B, int Hkv, int G, int D, int max_blocks_per_seq, int block_size, size_t P,
+                   bool allow_dynamic) {
+    if (!allow_dynamic || producers_for(D, G) != 1 || B > threads_for(D, G)) return 0;
+    const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
+    const long long tiles = static_cast<long long>(B) * Hkv * ((max_ctx + kTN - 1) / kTN);
+    if (tiles < static_cast<long long>(kDynMinTilesPerCta) * static_cast<long long>(P)) return 0;
+    return static_cast<int>(P) * kTailUnitsPerCta;
+}
+
+// Workspace layout: partials [units][2][G][D + 2] floats, records [units], the tail's counter.
+struct WsLayout {
+    size_t part, rec, ctr, total;
+};
+WsLayout ws_layout(size_t units, int G, int D) {
+    WsLayout w{};
+    w.part = 0;
+    w.rec = (units * 2 * G * (D + 2) * sizeof(float) + 255) / 256 * 256;
+    w.ctr = w.rec + (units * sizeof(SegRecord) + 15) / 16 * 16;
+    w.total = w.ctr + 16;
+    return w;
+}
+
+// a distinct, non-zero number per launch (records and the tail's counter carry it)
+unsigned next_epoch() {
+    static std::atomic<unsigned> e{0};
+    unsigned v = e.fetch_add(1u) + 1u;
+    if (v == 0) v = e.fetch_add(1u) + 1u;
+    return v;
+}
+
 }  // namespace
 
 DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, int block_size,
@@ -1287,8 +1533,8 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, in
     const int G = Hq / Hkv;
     const size_t P = static_cast<size_t>(device_sm_count()) *
                      launch_ctas_per_sm(B, Hq, Hkv, D, max_blocks_per_seq, block_size, allow_wide);
-    const size_t part = P * 2 * G * (D + 2) * sizeof(float);
-    plan.ws_bytes = (part + 255) / 256 * 256 + P * sizeof(SegRecord);
+    const size_t units = P + tail_units_for(B, Hkv, G, D, max_blocks_per_seq, block_size, P, allow_wide);
+    plan.ws_bytes = ws_layout(units, G, D).total;
     return plan;
 }
 
@@ -1314,10 +1560,14 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStrea
     prm.out = a.out;
     const int cps = launch_ctas_per_sm(a.B, a.Hq, a.Hkv, a.D, a.max_blocks, a.block_size, a.allow_wide);
     const size_t P = static_cast<size_t>(device_sm_count()) * cps;
-    const size_t part = P * 2 * G * (a.D + 2) * sizeof(float);
-    prm.part = static_cast<float *>(a.workspace);
-    prm.rec = reinterpret_cast<SegRecord *>(static_cast<char *>(a.workspace) + (part + 255) / 256 * 256);
-    (void)plan;
+    prm.tail_units = tail_units_for(a.B, a.Hkv, G, a.D, a.max_blocks, a.block_size, P, a.allow_wide);
+    const WsLayout w = ws_layout(P + prm.tail_units, G, a.D);
+    if (w.total > plan.ws_bytes) return cudaErrorInvalidValue;  // the plan and the launch disagree
+    char *ws = static_cast<char *>(a.workspace);
+    prm.part = reinterpret_cast<float *>(ws + w.part);
+    prm.rec = reinterpret_cast<SegRecord *>(ws + w.rec);
+    prm.ctr = reinterpret_cast<unsigned long long *>(ws + w.ctr);
+    prm.epoch = next_epoch();
     prm.err = a.err;
     prm.B = a.B;
     prm.Hq = a.Hq;
