@@ -55,8 +55,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # profiles/decode_kernel_qwen3_06b_decode.md and profiles/prefill_tc_kernel_prefill_prefix.md
 # (layer 0 of the default workload; prefill_prefix). Each is valid only for the kernel sources it
 # was taken on, identified by their hash; after any change the bench reports null.
-DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_283_083_776,
-                  "sha256": "572363a1d7f958faabcdce21184aa229a9bfdda5ea6448d02f69d18911a5104a"}
+DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_288_238_080,
+                  "sha256": "0c70c8f5c256a19f74f3dfe33db579ac306efbe425a0ab741fcb7fabcf93e089"}
 PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 411_290_112,
                    "sha256": "d7c18ebd78d322441abf0c57504a005c05546febc828c969fb144728954fb6a3"}
 
@@ -388,8 +388,9 @@ def run_gpu(args, ws_, rank, local):
     traffic = traffic_of(DECODE_TRAFFIC)
 
     # ---- e2e: inputs from pinned host memory each step, output read back each step ----
-    # through the C-ABI's host-buffer entry (pa_store_decode_host): the library queues one copy
-    # per input into its workspace, the fused store + decode, and the copy of the output back
+    # through the C-ABI's host-buffer entry (pa_store_decode_host): the library queues the
+    # transfer of the packed inputs into its workspace, the fused store + decode, and the
+    # transfer of the output back
     L = layers[0]
     c = L.c
     # the step's inputs sit in one pinned buffer at the library's packed offsets, as an engine's
