@@ -91,12 +91,13 @@ pa_status pa_store_kv(const void *k, const void *v, void *k_cache, void *v_cache
 
 /*
  * pa_decode_workspace_size: bytes of scratch pa_decode needs for these sizes on the current
- * device. The work is cut into units (one per CTA, one or two CTAs per SM; for group sizes up to
- * 3 and batches of at most 288 sequences, four more per CTA that CTAs take as they finish); each
- * unit has two partial results (G query heads x (D + 2) fp32: output, running max, sum) for the
- * at most two context pieces it shares with a neighbour, plus a 64-byte record, and the launch a
- * 16-byte counter. It depends on the group size G = Hq / Hkv, D, whether the batch fits one CTA's
- * threads and the SM count (about 4.9 MB at most on a GB300), not on the context lengths. Never
+ * device. The work is cut into units: one per CTA (one or two CTAs per SM), and, for group sizes
+ * up to 3 and batches of at most 9216 sequences whose tables could hold at least 16 tiles of 64
+ * positions per CTA, up to eight more per CTA that CTAs take as they finish.
+ * Each unit has two partial results (G query heads x (D + 2) fp32: output, running max, sum) for
+ * the at most two context pieces it shares with a neighbour, plus a 64-byte record; the launch a
+ * 16-byte counter. It depends on the group size G = Hq / Hkv, D, the batch size, the table's
+ * width and the SM count (about 12 MB at most on a GB300), not on the context lengths. Never
  * fails; returns 0 for sizes that pa_decode would reject.
  */
 size_t pa_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_blocks_per_seq,

@@ -85,14 +85,15 @@ constexpr int kWhole = 4;  // the segment is its pair's whole context: write the
 constexpr int kSlot1 = 8;  // partial segment that is not the unit's first: workspace slot 1
 constexpr int kEnd = 16;   // no tile: the CTA's work is done (dynamic tail)
 
-// Dynamic tail (one producer warp, batches of at most one CTA's threads). The launch's tiles
-// [0, F) are cut into one equal contiguous unit per CTA, as in the static scheme; the last
-// 1/kTailDiv of them, [F, total), into kTailUnitsPerCta units per CTA that CTAs take from a
-// counter as they finish, so that CTAs on slower SMs take fewer of them. All unit bounds are
-// closed-form, so the merge finds the pieces of a pair without a list.
+// Dynamic tail (kernels with one producer warp). The launch's tiles [0, F) are cut into one equal
+// contiguous unit per CTA, as in the static scheme; the last 1/kTailDiv of them, [F, total), into
+// K2 units (at most kTailUnitsPerCta per CTA) of 1/32 of a CTA's share, 2 to 8 tiles, that CTAs
+// take from a counter as they finish, so that CTAs on slower SMs take fewer of them. All unit
+// bounds are closed-form, so the merge finds the pieces of a pair without a list.
 constexpr int kTailDiv = 8;
-constexpr int kTailUnitsPerCta = 4;
-constexpr int kDynMinTilesPerCta = 64;  // smaller launches keep the static scheme
+constexpr int kTailUnitsPerCta = 8;
+constexpr int kDynMinTilesPerCta = 16;  // smaller launches keep the static scheme
+constexpr int kDynCoarse = 32;          // batches beyond one CTA's threads: offsets per 32 sequences
 
 struct TileMeta {
     int b, g, flags, all_valid;  // all_valid: every one of the 128 rows is a context position
@@ -182,7 +183,7 @@ struct Shape {
     }
 };
 
-// the dynamic tail's per-sequence tile offsets (int32, batches of at most one CTA's threads)
+// the dynamic tail's tile offsets (int32: one per sequence, or one per 32 sequences)
 __host__ __device__ constexpr int dyn_seq_bytes(int D, int G) {
     return producers_for(D, G) == 1 ? (threads_for(D, G) + 1 + 1) / 2 * 8 : 0;
 }
@@ -330,7 +331,8 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
     volatile int *abort_flag = reinterpret_cast<volatile int *>(scan + 20);
     PrepTile *prep = reinterpret_cast<PrepTile *>(scan + 24);  // [producers][kIdRing]
     int *idring = reinterpret_cast<int *>(prep + kProducers * kIdRing);  // [producers][kIdRing][TN]
-    int *seqpre = idring + kProducers * kIdRing * S::TN;  // dynamic tail: first tile of each sequence
+    int *seqpre = idring + kProducers * kIdRing * S::TN;  // dynamic tail: first tile of each
+                                                          // sequence (or of every 32nd)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = gridDim.x, cta = blockIdx.x;
@@ -393,7 +395,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
             scan[16] = tid;
             scan[17] = excl;
         }
-        if constexpr (dyn_seq_bytes(D, G) > 0) {
+        if constexpr (kProducers == 1) {
             if (total < (1ll << 31)) {  // the only case the dynamic tail runs in
                 if (tid < p.B) seqpre[tid] = static_cast<int>(excl);
                 if (tid == 0) seqpre[p.B] = static_cast<int>(total);
@@ -407,11 +409,14 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
         total = block_sum<kThreads>(mine, scan) * p.Hkv;
         lo = total * cta / P;
         hi = total * (cta + 1) / P;
+        // the dynamic tail needs the first tile of every 32nd sequence: pass 2 then runs to the end
+        const bool coarse = kProducers == 1 && p.tail_units > 0 && p.B <= kDynCoarse * kThreads &&
+                            total < (1ll << 31) && total >= static_cast<long long>(kDynMinTilesPerCta) * P;
 
         // ---- pass 2: the (b, g, t) of tile `lo` ----
         if (tid == 0) scan[16] = -1;
         __syncthreads();
-        if (lo < hi) {
+        if (lo < hi || coarse) {
             long long running = 0;  // tiles of sequences before this chunk, times Hkv
             for (int base = 0; base < p.B; base += kThreads) {
                 const int b = base + tid;
@@ -429,34 +434,39 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                     chunk_total += scan[i];
                 }
                 const long long excl = running + (before + v - nt) * p.Hkv;
-                if (nt > 0 && excl <= lo && lo < excl + static_cast<long long>(nt) * p.Hkv) {
+                if (lo < hi && nt > 0 && excl <= lo && lo < excl + static_cast<long long>(nt) * p.Hkv) {
                     scan[16] = b;
                     scan[17] = excl;
                 }
+                if (coarse && b < p.B && b % kDynCoarse == 0) seqpre[b / kDynCoarse] = static_cast<int>(excl);
                 running += chunk_total * p.Hkv;
                 __syncthreads();
-                if (running > lo) break;  // uniform: every thread sees the same `running`
+                if (!coarse && running > lo) break;  // uniform: every thread sees the same `running`
             }
+            if (coarse && tid == 0) seqpre[(p.B + kDynCoarse - 1) / kDynCoarse] = static_cast<int>(total);
         }
         __syncthreads();
     }
     const int b0 = static_cast<int>(scan[16]);
     const long long seq_start = scan[17];  // global index of tile (b0, 0, 0)
 
-    // the dynamic tail runs for large enough batches of at most one CTA's threads (its offsets
-    // per sequence live in shared memory) when the workspace holds its units; the choice is the
-    // same in every CTA
+    // the dynamic tail runs for large enough launches of at most 32 CTAs' threads of sequences
+    // (their tile offsets, per sequence or per 32 sequences, live in shared memory) when the
+    // workspace holds its units; the choice is the same in every CTA
     bool dyn = false;
     long long F = total;
     int K2 = 0;
-    if constexpr (dyn_seq_bytes(D, G) > 0) {
-        if (p.tail_units > 0 && p.B <= kThreads && total < (1ll << 31) &&
-            total >= static_cast<long long>(kDynMinTilesPerCta) * P) {
-            dyn = true;
-            K2 = p.tail_units;
-            F = total - total / kTailDiv;
-        }
+    if (kProducers == 1 && p.tail_units > 0 && p.B <= kDynCoarse * kThreads && total < (1ll << 31) &&
+        total >= static_cast<long long>(kDynMinTilesPerCta) * P) {
+        F = total - total / kTailDiv;
+        const long long per_cta = total / P;  // tiles of a CTA's share
+        const long long chunk = per_cta / 32 < 2 ? 2 : (per_cta / 32 > 8 ? 8 : per_cta / 32);
+        const long long k2 = (total - F + chunk - 1) / chunk;
+        K2 = static_cast<int>(k2 < p.tail_units ? k2 : p.tail_units);
+        dyn = K2 > 0;
+        if (!dyn) F = total;
     }
+    const bool exact_seq = p.B <= kThreads;  // seqpre holds every sequence's first tile
     auto make_rec = [&](long long ulo, long long uhi) {
         SegRecord r{};
         r.lo = ulo;
@@ -499,10 +509,12 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
         const int R = p.box_rows, nbox = TN / R;
         const uint32_t box_bytes = static_cast<uint32_t>(R) * D * 2;
         const unsigned long long box_rows_mask = R == 64 ? ~0ull : ((1ull << R) - 1ull);
-        // The unit being walked: `u_count` tiles from tile u_lo of the launch; the walker
-        // (b, g, t) is the next tile to prepare, `u_pos` its index in the unit. The unit's first
-        // segment is its tiles [0, first_len); it began inside its pair if first_mid.
-        long long unit = cta, u_count = 0, u_pos = 0, first_len = 0;
+        // The unit being walked: `u_count` tiles; the walker (b, g, t) is the next tile to
+        // prepare, `u_pos` its index in the unit. The unit's first segment is its tiles
+        // [0, first_len); it began inside its pair if first_mid. With the dynamic tail (one
+        // producer) the CTA's stream of tiles runs through unit after unit; `stream_total` counts
+        // the tiles of the units taken so far.
+        long long unit = cta, u_count = 0, u_pos = pw, first_len = 0, stream_total = 0;
         bool first_mid = false, done = false, took_static = false, ticket_ready = false;
         int b = 0, nt = 1, n = 0, g = 0, t = 0;
         auto seed = [&](int sb, long long sstart, long long X, long long cnt) {
@@ -513,7 +525,6 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
             g = static_cast<int>(off / nt);
             t = static_cast<int>(off % nt);
             u_count = cnt;
-            u_pos = 0;
             first_len = min(cnt, static_cast<long long>(nt - t));
             first_mid = t > 0;
         };
@@ -533,18 +544,43 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
         auto unit_lo = [&](long long v) -> long long {
             return v <= P ? F * v / P : F + (total - F) * (v - P) / K2;
         };
-        // dynamic tail: the sequence holding tile X (offsets are non-decreasing, seqpre[B] = total)
-        auto find_seq = [&](long long X) -> int {
-            int l = 0, h = p.B;
+        // dynamic tail: the sequence holding tile X and its first tile (offsets are
+        // non-decreasing). Per-sequence offsets: a binary search. Offsets per 32 sequences: a
+        // binary search for the group, then one warp-wide read of the group's lengths. Warp-uniform.
+        auto find_seq = [&](long long X, long long &soff) -> int {
+            if (exact_seq) {
+                int l = 0, h = p.B;  // seqpre[l] <= X < seqpre[h]
+                while (h - l > 1) {
+                    const int mid = (l + h) >> 1;
+                    if (seqpre[mid] <= X) l = mid;
+                    else h = mid;
+                }
+                soff = seqpre[l];
+                return l;
+            }
+            int l = 0, h = (p.B + kDynCoarse - 1) / kDynCoarse;
             while (h - l > 1) {
                 const int mid = (l + h) >> 1;
                 if (seqpre[mid] <= X) l = mid;
                 else h = mid;
             }
-            return l;
+            const int bb = l * kDynCoarse + lane;
+            const int ntl = bb < p.B ? ntiles_of<S::TN>(p, bb, cap) : 0;
+            int incl = ntl;  // inclusive scan over the group
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const long long ex = seqpre[l] + static_cast<long long>(incl - ntl) * p.Hkv;
+            // the group holds tile X, so its first sequence with tiles starts at or before X
+            const unsigned m = __ballot_sync(kFull, ntl > 0 && ex <= X);
+            const int ln = 31 - __clz(m);
+            soff = __shfl_sync(kFull, ex, ln);
+            return l * kDynCoarse + ln;
         };
-        // dynamic tail: move the walker to the next unit that holds tiles (first the CTA's static
-        // one, then tickets); records every unit taken, empty ones included. Warp-uniform.
+        // dynamic tail: move the walker to the first tile of the next unit that holds tiles, or
+        // set `done`: the CTA's static unit first, then tickets. Records every unit taken (empty
+        // ones included). Warp-uniform.
         auto next_unit = [&]() {
             for (;;) {
                 long long v;
@@ -556,15 +592,11 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                     if (lane == 0)
                         tk = take_ticket(p.ctr, reinterpret_cast<unsigned *>(p.ctr + 1), p.epoch, ticket_ready);
                     tk = __shfl_sync(kFull, tk, 0);
-                    if (tk < 0) {
-                        if (lane == 0) {
-                            raise_err(p.err, PA_DEVERR_TIMEOUT);
-                            *abort_flag = 1;
-                        }
-                        done = true;
-                        return;
+                    if (tk < 0 && lane == 0) {
+                        raise_err(p.err, PA_DEVERR_TIMEOUT);
+                        *abort_flag = 1;
                     }
-                    if (tk >= K2) {
+                    if (tk < 0 || tk >= K2) {
                         done = true;
                         return;
                     }
@@ -573,13 +605,14 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
                 const long long vlo = unit_lo(v), vhi = unit_lo(v + 1);
                 SegRecord r = make_rec(vlo, vhi);
                 if (vlo < vhi) {
-                    const int sb = find_seq(vlo);
-                    seed(sb, seqpre[sb], vlo, vhi - vlo);
+                    long long soff;
+                    const int sb = find_seq(vlo, soff);
+                    seed(sb, soff, vlo, vhi - vlo);
                     unit = v;
                     r.b = b;
                     r.g = g;
                     r.ntiles = nt;
-                    r.pair_start = seqpre[sb] + static_cast<long long>(g) * nt;
+                    r.pair_start = soff + static_cast<long long>(g) * nt;
                 }
                 if (lane == 0) p.rec[v] = r;
                 if (vlo < vhi) return;
@@ -588,7 +621,6 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
         if (!dyn) {
             seed(b0, seq_start, lo, count);
             for (int k = 0; k < pw && k < count; ++k) advance();
-            u_pos = pw;
         }
         PrepTile *myprep = prep + pw * kIdRing;
         int *myids = idring + pw * kIdRing * TN;
@@ -599,7 +631,16 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
         // group per lane. With the dynamic tail a step past the CTA's last tile records "no tile".
         auto prepare = [&](long long j) {
             const int sl = static_cast<int>(j % kIdRing);
-            if (dyn && !done && u_pos == u_count) next_unit();
+            // past the unit: on to the next, at the same distance beyond its start
+            while (dyn && !done && u_pos >= u_count) {
+                const long long carry = u_pos - u_count;
+                next_unit();
+                if (done) break;
+                stream_total += u_count;
+                u_pos = carry;
+                if (carry < u_count)
+                    for (long long c = 0; c < carry; ++c) advance();
+            }
             if (done) {
                 if (lane == 0) myprep[sl].b = -1;
                 cp_async_commit();
@@ -801,10 +842,12 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
             }
         }
         __syncwarp();
-        if (dyn && !aborted) {
-            // tell the consumers there is nothing more: the next stage, with no bytes and the end
-            // flag (after the drain above, whose waits would not see phases this one completes)
-            const long long i = j;
+        const long long i_end = pw + static_cast<long long>(kProducers) * j;
+        if (dyn && !aborted && i_end == stream_total) {
+            // tell the consumers there is nothing more: the stage after the last tile (this
+            // producer's, as its predecessor in that stage was), with no bytes and the end flag,
+            // after the drain above, whose waits would not see phases this one completes
+            const long long i = i_end;
             const int stage = static_cast<int>(i % NS);
             const uint32_t phase = static_cast<uint32_t>((i / NS) & 1);
             if (warp_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
@@ -888,7 +931,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
         float m_run = -INFINITY, l_part = 0.f;
         int stage = 0;
         uint32_t phase = 0;
-        for (long long i = 0; i < count; ++i) {
+        for (long long i = 0; dyn || i < count; ++i) {
             const bool ok = warp_wait(full0 + 8 * stage, phase, abort_flag);
             if (!ok) {
                 if (lane == 0) {
@@ -899,6 +942,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
             }
             const TileMeta &m = metas[stage];
             const int mflags = m.flags, mb = m.b, mg = m.g, mall = m.all_valid, mnew = m.newrow, munit = m.unit;
+            if (mflags & kEnd) break;  // dynamic tail: the CTA's work is done
             const unsigned char *st = ring + static_cast<size_t>(stage) * S::STAGE_BYTES;
             const uint32_t kb = smem_addr(st), vb = kb + S::TILE_BYTES;
 
@@ -1492,12 +1536,12 @@ int launch_ctas_per_sm(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, in
 }
 
 // Units of the dynamic tail a launch's workspace holds: for the kernels with one producer warp and
-// batches of at most one CTA's threads whose table could hold enough tiles per CTA (an upper
-// bound: every sequence at the table's full length; the kernel decides on the real count); none
-// when the caller's scratch is fixed (allow_dynamic false).
+// batches of at most 32 CTAs' threads of sequences whose table could hold enough tiles per CTA (an
+// upper bound: every sequence at the table's full length; the kernel decides on the real count);
+// none when the caller's scratch is fixed (allow_dynamic false).
 int tail_units_for(int B, int Hkv, int G, int D, int max_blocks_per_seq, int block_size, size_t P,
                    bool allow_dynamic) {
-    if (!allow_dynamic || producers_for(D, G) != 1 || B > threads_for(D, G)) return 0;
+    if (!allow_dynamic || producers_for(D, G) != 1 || B > kDynCoarse * threads_for(D, G)) return 0;
     const long long max_ctx = static_cast<long long>(max_blocks_per_seq) * block_size;
     const long long tiles = static_cast<long long>(B) * Hkv * ((max_ctx + kTN - 1) / kTN);
     if (tiles < static_cast<long long>(kDynMinTilesPerCta) * static_cast<long long>(P)) return 0;

@@ -248,18 +248,28 @@ def _fused_step(c):
     return out, kc, vc
 
 
-@pytest.mark.parametrize("G,Hkv,D,bs,dt,B,lo,hi", [(2, 8, 128, 256, "bf16", 64, 2800, 4096),
-                                                   (1, 4, 64, 16, "f16", 240, 1800, 2600),
-                                                   (3, 2, 128, 16, "bf16", 280, 2800, 4000)])
+@pytest.mark.parametrize("G,Hkv,D,bs,dt,B,lo,hi", [
+    (2, 8, 128, 256, "bf16", 64, 2800, 4096),   # one producer, offsets per sequence
+    (1, 4, 64, 16, "f16", 240, 1800, 2600),
+    (3, 2, 128, 16, "bf16", 280, 2800, 4000),
+    (2, 2, 64, 16, "f16", 600, 1200, 2000),     # one producer, offsets per 32 sequences
+    (4, 2, 128, 256, "bf16", 128, 2500, 4000),  # tensor-core consumers: equal shares only
+    (8, 1, 128, 16, "bf16", 160, 2000, 3000),
+    (7, 2, 64, 16, "f16", 256, 1500, 3000),
+    (8, 2, 128, 256, "bf16", 700, 600, 1200),
+])
 def test_dynamic_tail_elementwise(orc, G, Hkv, D, bs, dt, B, lo, hi):
-    """Launches with many tiles per CTA on the one-producer kernels (GQA groups up to 3, at most
-    one CTA's threads of sequences) split their last eighth of tiles into small units that CTAs
-    take from a counter as they finish. Unit bounds are closed-form and each unit's arithmetic is
-    the same whichever CTA runs it, so the output is checked element by element against the
-    oracle and must be bit-identical between the two-call step and the fused call, and between
-    repeated calls."""
+    """Launches of the one-producer kernels (groups up to 3) with enough tiles per CTA split their
+    last eighth of tiles into small units that CTAs take from a counter as they finish (beyond one
+    CTA's threads of sequences the first tile of every 32nd sequence is kept and a unit's sequence
+    is found by one warp-wide read). Unit bounds are closed-form and each unit's arithmetic is the
+    same whichever CTA runs it, so the output is checked element by element against the oracle and
+    must be bit-identical between the two-call step and the fused call, and between repeated calls;
+    the same for the tensor-core kernels at the same sizes, which keep equal shares. Empty
+    sequences are mixed in."""
     rng = np.random.default_rng(B + G)
     lens = rng.integers(lo, hi, size=B, endpoint=True)
+    lens[rng.choice(B, size=max(1, B // 40), replace=False)] = 0
     c = W.decode_case(B=B, Hq=G * Hkv, Hkv=Hkv, D=D, block_size=bs, dtype=dt, context_lens=lens,
                       seed=B + 7)
     _check_full(orc, c)
