@@ -55,8 +55,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # profiles/decode_kernel_qwen3_06b_decode.md and profiles/prefill_tc_kernel_prefill_prefix.md
 # (layer 0 of the default workload; prefill_prefix). Each is valid only for the kernel sources it
 # was taken on, identified by their hash; after any change the bench reports null.
-DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_288_238_080,
-                  "sha256": "0c70c8f5c256a19f74f3dfe33db579ac306efbe425a0ab741fcb7fabcf93e089"}
+DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_290_084_096,
+                  "sha256": "21cce5f9d8ea2f2170c0f450e2ce15a5a7de0635d4ee751eb8ddab2203eb7482"}
 PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 411_290_112,
                    "sha256": "d7c18ebd78d322441abf0c57504a005c05546febc828c969fb144728954fb6a3"}
 
