@@ -161,19 +161,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const long long idx = static_cast<long long>(__shfl_sync(kFull, nxt, 0));
             if (idx >= p.n_items) break;
             if (lane == 0) nxt = atomicAdd(p.sched, 1ull);  // in flight while this one is resolved
-            const long long per_seq = static_cast<long long>(p.pairs) * p.row_blocks;
-            const int s = static_cast<int>(idx / per_seq);
-            const int rem = static_cast<int>(idx % per_seq);
-            const int pair = rem / p.row_blocks;
-            const int mb = p.row_blocks - 1 - rem % p.row_blocks;  // most keys first
+            // tickets by rank r of a row block counted from its prompt's last one (the block with
+            // the most keys), then prompt, then pair: large items first across the whole launch,
+            // and the last ones handed out are the first row blocks of long prompts, the smallest
+            const long long per_rank = static_cast<long long>(p.S) * p.pairs;
+            const int r = static_cast<int>(idx / per_rank);
+            const int rem = static_cast<int>(idx % per_rank);
+            const int s = rem / p.pairs;
+            const int pair = rem % p.pairs;
             const int q0 = p.cu_q[s], ql = p.cu_q[s + 1] - q0;
             const int k0 = p.cu_k[s], kl = p.cu_k[s + 1] - k0;
             if (ql < 0 || ql > p.max_seqlen_q) {
-                if (mb == 0 && pair == 0 && lane == 0) raise_err(p.err, PA_DEVERR_LENGTH);
+                if (r == 0 && pair == 0 && lane == 0) raise_err(p.err, PA_DEVERR_LENGTH);
                 continue;
             }
+            const int mb = (ql + BM - 1) / BM - 1 - r;  // row block of this rank
+            if (mb < 0) continue;
             const int m0 = mb * BM;
-            if (m0 >= ql) continue;
             const int mrows = min(BM, ql - m0);
             const int32_t *trow =
                 p.block_tables ? p.block_tables + static_cast<size_t>(s) * p.max_blocks : nullptr;
