@@ -7,13 +7,16 @@
 // Decode reads every cached K/V row once and does ~G multiply-adds per byte, far below the HBM
 // ridge, so the kernel is organised to keep HBM streaming, not to reach the tensor cores.
 //
-// Work: the flattened space of 128-position tiles over (sequence b, kv head g, tile t), ordered
-// b, then g, then t, is cut into one equal contiguous range per CTA (one persistent CTA per SM),
-// so every SM streams the same number of bytes and no CTA is a straggler. A CTA's range covers
-// whole (b, g) pairs plus at most a partial pair at each end ("segments").
+// Work: the flattened space of 64-position tiles (128 on the tensor-core path at D = 64) over
+// (sequence b, kv head g, tile t), ordered b, then g, then t, is cut into units of contiguous
+// tiles: one equal range per persistent CTA (one or two CTAs per SM), so every SM streams about
+// the same number of bytes; with one producer warp the last eighth of the tiles is cut into small
+// units instead, which CTAs take from a counter as they finish (the dynamic tail), so CTAs on
+// slower SMs take fewer of them. A unit covers whole (b, g) pairs plus at most a partial pair at
+// each end ("segments"); the merge kernel combines the pieces of pairs split between units.
 //
-// CTA = 1 producer warp + 8 consumer warps.
-//  * Producer: walks the range; for each tile it looks the rows' physical blocks up in the block
+// CTA = 1 or 2 producer warps + 8 consumer warps.
+//  * Producer: walks its units; for each tile it looks the rows' physical blocks up in the block
 //    table and issues TMA loads of the K and V tile rows (one box per run of `box_rows` rows that
 //    share a block) into a ring of shared-memory stages, plus a bulk copy of the G query rows at
 //    the start of each segment. full/empty mbarriers hand stages to and from the consumers; the
@@ -25,7 +28,7 @@
 //    disjoint banks of the unswizzled tile. Online softmax in base 2 per warp; PV with each lane
 //    owning 8 output columns. At a segment's end the 8 warps' (max, sum, O) are combined: a
 //    segment covering its whole pair writes the output; a partial segment writes (O/sum, max,
-//    sum) to one of the CTA's two workspace slots, and decode_merge_kernel combines the pieces.
+//    sum) to one of its unit's two workspace slots, and decode_merge_kernel combines the pieces.
 //  * Consumers, large groups (G >= 4): at ~G multiply-adds per byte the fp32 pipes, not HBM,
 //    would set the pace, so the G heads of one KV head go through the warp-level tensor-core
 //    path as the M rows of a 16-row fragment (heads G..15 are zero). Per warp and tile:
