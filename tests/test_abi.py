@@ -183,3 +183,18 @@ def test_store_decode_host_layout(lib):
     assert lib.pa_store_decode_host_layout(B, Hq, Hkv, D, maxb, None) == n
     assert binding.pa_store_decode_host_layout(0, Hq, Hkv, D, maxb) == (None, 0)
     assert binding.pa_store_decode_host_layout(B, 5, Hkv, D, maxb) == (None, 0)
+
+
+def test_workspace_units_rules(lib):
+    """The decode workspace holds one unit per CTA, plus up to eight per CTA of the dynamic tail
+    for group sizes up to 3 when the batch has at most 9216 sequences and its table could hold
+    enough tiles; the static scheme's size does not depend on the batch."""
+    ws = lib.pa_decode_workspace_size
+    # group of 8: equal shares only, whatever the batch and table
+    assert ws(8, 16, 2, 128, 64, 256) == ws(256, 16, 2, 128, 64, 256) == ws(256, 16, 2, 128, 1, 1)
+    # group of 2: a table too narrow for the tail, a wide one, and a batch beyond 9216 sequences
+    static = ws(256, 16, 8, 128, 1, 1)
+    wide = ws(256, 16, 8, 128, 64, 256)
+    assert 8.0 < wide / static < 10.0
+    assert ws(10000, 16, 8, 128, 64, 256) == static
+    assert ws(9216, 16, 8, 128, 64, 256) == wide
