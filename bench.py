@@ -56,7 +56,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (layer 0 of the default workload; prefill_prefix). Each is valid only for the kernel sources it
 # was taken on, identified by their hash; after any change the bench reports null.
 DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_290_084_096,
-                  "sha256": "f046a3dedbb8a3f4c0cf725a4d93296f97c88703123e1f9ac3f83f6aec615a57"}
+                  "sha256": "ac07fccc7c7f9b0d61a556c3c2b5480066451d1d27d9fb3b6c224da93438bef5"}
 PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 699_134_976,
                    "sha256": "bc2aa36307645f2b743031ee20edb4d4d1480634c459f3d96973e9c06ba665b3"}
 

@@ -1270,7 +1270,7 @@ __global__ void __launch_bounds__(threads_for(D, G), CPS) decode_kernel(const __
 // which of each one's two partial slots holds the pair) follows from this unit's own record with
 // no further reads. After that record, every global read the result depends on (each segment's
 // max, sum and partial row) is issued together: two memory round trips for up to kMergeChunk
-// segments. Records another launch left (older epoch) are ignored.
+// segments. Records this launch did not write are ignored.
 constexpr int kMergeMaxCtas = 512;  // decode CTAs per launch (2 per SM at most)
 constexpr int kMergeThreads = 256;
 constexpr int kMergeBatch = 512;    // contributing units listed at a time
@@ -1288,9 +1288,18 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const __gri
     // launched ahead of time (programmatic dependent launch): wait until the decode grid has
     // completed and its writes are visible
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the decode grid is done with the tail's counter: clear its tag, so that the next launch on
+    // this workspace resets the counter even when it carries the same epoch (a replayed graph)
+    if (c == 0 && tid == 0) p.ctr[0] = 0ull;
     const SegRecord rc = p.rec[c];
-    if (rc.epoch != p.epoch || rc.b < 0 || rc.b >= p.B || rc.g < 0 || rc.g >= p.Hkv || rc.P < 1 ||
-        rc.K2 < 0 || (rc.K2 == 0 && c >= rc.P) || rc.total <= 0)
+    // unit 0's record is written by every launch: a record this launch did not write (another
+    // launch's, or one from an earlier replay of the same graph) disagrees with it or lies past
+    // the launch's units
+    const SegRecord r0 = p.rec[0];
+    if (rc.epoch != p.epoch || r0.epoch != p.epoch || rc.total != r0.total || rc.F != r0.F ||
+        rc.P != r0.P || rc.K2 != r0.K2 || c >= r0.P + r0.K2)
+        return;
+    if (rc.b < 0 || rc.b >= p.B || rc.g < 0 || rc.g >= p.Hkv || rc.P < 1 || rc.K2 < 0 || rc.total <= 0)
         return;
     if (rc.pair_start >= rc.lo || rc.pair_start + rc.ntiles > rc.hi) return;
     const long long x = rc.pair_start, total = rc.total, F = rc.F;

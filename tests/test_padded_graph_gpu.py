@@ -81,3 +81,57 @@ def test_padded_bucket_graph_replays(orc, Hq, Hkv, D, DT, fused):
         e = max_abs(o[:n_real], ref)
         assert e <= TOL[DT], (n_real, e)
         assert np.all(o[n_real:] == 0.0), n_real  # padding rows: zeros, not stale values
+
+
+def test_graph_replays_with_and_without_the_dynamic_tail(orc):
+    """A graph replays the same launch parameters (the same launch epoch) every time, while the
+    real batch in its buffers changes: replays whose tile count turns the dynamic tail on must get
+    a fresh ticket counter each time, and a replay that runs equal shares only must not merge the
+    tail records an earlier replay left in the workspace."""
+    bucket, maxb, bs, nb, Hq, Hkv, D, DT = 128, 64, 16, 8400, 16, 8, 64, "f16"
+
+    def batch(n_real, seed, lo):
+        rng = np.random.default_rng([seed, 9])
+        ctx = np.zeros(bucket, np.int64)
+        ctx[:n_real] = rng.integers(lo, maxb * bs, size=n_real, endpoint=True)
+        return W.decode_case(B=bucket, Hq=Hq, Hkv=Hkv, D=D, block_size=bs, dtype=DT, context_lens=ctx,
+                             num_blocks=nb, max_blocks_per_seq=maxb, seed=seed)
+
+    c0 = batch(bucket, 11, 700)
+    bufs = {"q": to_dev(c0.q, DT), "kn": to_dev(c0.k_new, DT), "vn": to_dev(c0.v_new, DT),
+            "kc": to_dev(c0.k_cache, DT), "vc": to_dev(c0.v_cache, DT),
+            "bt": i32(c0.block_tables), "cl": i32(c0.context_lens)}
+    out = torch.empty_like(bufs["q"])
+    ws = workspace(bucket, Hq, Hkv, D, maxb, bs)
+    err = err_buf()
+
+    def body():
+        pa.pa_store_decode(out, bufs["q"], bufs["kn"], bufs["vn"], bufs["kc"], bufs["vc"], bufs["bt"],
+                           bufs["cl"], c0.scale, workspace=ws, err=err)
+
+    body()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        body()
+    # full batches of long contexts (about 14 k tiles: the tail runs), then a small batch (equal
+    # shares), then full batches again
+    for n_real, seed, lo in [(bucket, 12, 700), (16, 13, 1), (bucket, 14, 700), (bucket, 15, 900),
+                             (8, 16, 1), (bucket, 12, 700)]:
+        c = batch(n_real, seed, lo)
+        for key, a in (("q", c.q), ("kn", c.k_new), ("vn", c.v_new), ("kc", c.k_cache), ("vc", c.v_cache)):
+            bufs[key].copy_(to_dev(a, DT))
+        bufs["bt"].copy_(i32(c.block_tables))
+        bufs["cl"].copy_(i32(c.context_lens))
+        out.fill_(float("nan"))
+        err.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        kref, vref = orc.store_kv(c.k_new, c.v_new, c.k_cache, c.v_cache, c.slot_mapping)
+        assert np.array_equal(bits(bufs["kc"]), kref) and np.array_equal(bits(bufs["vc"]), vref)
+        o = f64(out)
+        ref = orc.decode(c.q[:n_real], kref, vref, c.block_tables[:n_real], c.context_lens[:n_real],
+                         scale=c.scale, dtype=DT)
+        assert max_abs(o[:n_real], ref) <= TOL[DT]
+        assert not o[n_real:].any()  # padding rows are zero
