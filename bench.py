@@ -51,10 +51,9 @@ METRIC = "paged-decode KV-read GB/s (% of GB300 HBM peak); decode steps/sec per 
 DEFAULT_WORKLOAD = "qwen3_06b_decode"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic (read + write bytes) of one launch, from the ncu captures summarised in
-# profiles/decode_kernel_qwen3_06b_decode.md and profiles/prefill_tc_kernel_prefill_prefix.md
-# (layer 0 of the default workload; prefill_prefix). Each is valid only for the kernel sources it
-# was taken on, identified by their hash; after any change the bench reports null.
+# DRAM traffic (read + write bytes) of one launch, from the ncu captures of these kernels (layer 0
+# of the default workload; prefill_prefix). Each is valid only for the kernel sources it was taken
+# on, identified by their hash; after any change the bench reports null.
 DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_290_084_096,
                   "sha256": "ac07fccc7c7f9b0d61a556c3c2b5480066451d1d27d9fb3b6c224da93438bef5"}
 PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 699_134_976,
@@ -89,6 +88,22 @@ def src_hash(*names: str) -> str:
 
 def traffic_of(rec: dict):
     return rec["bytes"] if src_hash(*rec["sources"]) == rec["sha256"] else None
+
+
+def step_config(workload: str, n_layers: int, world: int) -> dict:
+    """The ``config`` object of the JSON line: the workload one step runs (rank 0's layers),
+    computed from its lengths alone, so that both arms print the same keys and values."""
+    w = W.CONFIGS[workload]
+    p = w.params
+    nbytes = [kv_bytes(W.lengths(workload, rank_seed(w.seed, 0, l)), p["Hkv"], p["D"])
+              for l in range(n_layers)]
+    mean = statistics.mean(nbytes)
+    return {"workload": workload, "seqs": int(len(W.lengths(workload, w.seed))), "Hq": p["Hq"],
+            "Hkv": p["Hkv"], "D": p["D"], "block_size": p["block_size"],
+            "kv_bytes_per_step": int(mean), "layers_rotated": n_layers,
+            "l2": f"inputs larger than L2: each step reads a {mean / 1e9:.1f} GB KV set of its own "
+                  f"layer ({n_layers} layers alternate)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -257,10 +272,11 @@ def run_reference(args, ws_, rank):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws_,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.workload, "seqs_per_step": len(rows)},
+            "data": "synthetic", "config": step_config(args.workload, args.layers, ws_),
             "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle",
                              "cores": orc.max_threads(),
-                             "sample": f"{len(rows)} of {case.B} sequences of {case.name} per step"},
+                             "sample": f"{len(rows)} of {case.B} sequences of {case.name} (layer 0) "
+                                       f"per step, fp64"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -306,7 +322,19 @@ def run_gpu(args, ws_, rank, local):
     stream = torch.cuda.current_stream()
     pk, pk_kind = peaks()
     hbm = float(pk["hbm_gbs"])
-    bf16_peak = float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"]))
+    # the prefill kernel is timed alone (L2 flushed around it): its fraction is of the burst peak
+    bf16_peak = float(pk["bf16_tflops"])
+    bf16_sustained = float(pk.get("bf16_tflops_sustained", bf16_peak))
+
+    if args.only == "prefill":
+        # the prefill row alone (store + varlen prefill on prefill_prefix): a short command for
+        # profiling those two kernels without the decode pools on the device
+        rows = bench_prefill(torch, pa, dev, stream, bf16_peak, bf16_sustained, hbm, args, pk_kind)
+        if rank == 0:
+            print(json.dumps({"rows": rows}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
 
     # ---- inputs: two layers of the decode workload (seeds differ per layer and rank) ----
     base = W.CONFIGS[args.workload].seed
@@ -457,7 +485,8 @@ def run_gpu(args, ws_, rank, local):
     # ---- other rows: prefill with a cached prefix (store + varlen prefill) ----
     rows = {}
     if not args.skip_prefill:
-        rows.update(bench_prefill(torch, pa, dev, stream, bf16_peak, hbm, args))
+        rows.update(bench_prefill(torch, pa, dev, stream, bf16_peak, bf16_sustained, hbm, args,
+                                  pk_kind))
     if not args.skip_small:
         rows["decode_small_graphs"] = bench_small_decode(torch, pa, dev, hbm)
     if not args.skip_groups:
@@ -506,13 +535,7 @@ def run_gpu(args, ws_, rank, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws_, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": c0.dtype, "data": "synthetic",
-        "config": {"workload": args.workload, "seqs": c0.B, "Hq": c0.Hq, "Hkv": c0.Hkv,
-                   "D": c0.D, "block_size": c0.block_size,
-                   "kv_bytes_per_step": int(statistics.mean(nbytes)),
-                   "layers_rotated": nl,
-                   "l2": f"inputs larger than L2: each step reads a {statistics.mean(nbytes) / 1e9:.1f} GB "
-                         f"KV set of its own layer ({nl} layers alternate)",
-                   "parallelism": f"replicas x{ws_}" if ws_ > 1 else "single GPU"},
+        "config": step_config(args.workload, nl, ws_),
         "pct_of_hbm_peak": 100.0 * value / hbm / ws_,
         "decode_steps_per_sec_per_layer": 1e3 / ms_step,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -703,7 +726,7 @@ def bench_block_manager(pa) -> dict:
     return out
 
 
-def bench_prefill(torch, pa, dev, stream, bf16_peak, hbm, args) -> dict:
+def bench_prefill(torch, pa, dev, stream, bf16_peak, bf16_sustained, hbm, args, pk_kind) -> dict:
     c = W.make("prefill_prefix")
     i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
     kc, vc = to_dev(torch, c.k_cache, c.dtype, dev), to_dev(torch, c.v_cache, c.dtype, dev)
@@ -739,7 +762,10 @@ def bench_prefill(torch, pa, dev, stream, bf16_peak, hbm, args) -> dict:
     return {"prefill": {"workload": "prefill_prefix", "kernel": "prefill_tc_kernel",
                         "ms": pf, "TFLOP_per_s": flops / (pf * 1e-3) / 1e12,
                         "frac_of_bf16_peak": flops / (pf * 1e-3) / 1e12 / bf16_peak,
-                        "peak": bf16_peak, "flops": flops, "l2": "flushed between iterations",
+                        "peak": bf16_peak, "peak_source": f"{pk_kind} bf16_tflops (burst: the "
+                                                          f"kernel is timed alone)",
+                        "frac_of_bf16_sustained": flops / (pf * 1e-3) / 1e12 / bf16_sustained,
+                        "flops": flops, "l2": "flushed between iterations",
                         "traffic": traffic_of(PREFILL_TRAFFIC)},
             "store_kv_prefill": {"kernel": "store_kv_kernel", "ms": st, "bytes": st_bytes,
                                  "GB_per_s": st_bytes / (st * 1e-3) / 1e9,
@@ -765,6 +791,8 @@ def main():
     ap.add_argument("--layers", type=int, default=2, help="layers whose pools alternate")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clock-tail", action="store_true")
+    ap.add_argument("--only", choices=["prefill"], default=None,
+                    help="run one row alone (no headline line): for profiling its kernels")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -104,6 +104,16 @@ size_t pa_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_blocks_pe
                                 int block_size);
 
 /*
+ * pa_decode_debug_tail_units: diagnostics (the pages have no counterpart). Once the last
+ * pa_decode or pa_store_decode launch that used `workspace` (with these sizes) has completed, the
+ * number of dynamic-tail units that launch ran: 0 when it kept one equal share per CTA. Read from
+ * the launch's own record in the workspace with a synchronous 64-byte device-to-host copy.
+ * Returns -1 for sizes pa_decode would reject, a NULL workspace or a failed copy.
+ */
+int pa_decode_debug_tail_units(const void *workspace, int B, int Hq, int Hkv, int D,
+                               int max_blocks_per_seq, int block_size);
+
+/*
  * pa_decode: paged grouped-query decode attention, one query token per sequence.
  *
  * Source: "nano-vLLM Part 4" section 3 (decode: one already-sampled token per sequence;
@@ -263,8 +273,10 @@ pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void 
  *   PA_DECODE_NOALLOC_SCRATCH_BYTES (GQA groups of 8 at D = 128, for instance) are rejected with
  *   PA_ERR_WORKSPACE before anything is launched (use pa_decode for them).
  * - Set-up: the first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call before any stream
- *   capture. A failed lookup returns PA_ERR_CUDA.
+ *   (cudaGetSymbolAddress) with that device current and keeps it for the life of the process;
+ *   make that first call before any stream capture. A failed lookup returns PA_ERR_CUDA. A
+ *   cudaDeviceReset (or any reset of the device's primary context) invalidates the kept address:
+ *   do not call pa_decode_noalloc on a device after resetting it.
  * - Sharing: every call on a device uses the same array and leaves the last call's partial
  *   results in it. Nothing in it needs to start at zero, but calls that overlap on the GPU
  *   (on different streams, or from different host threads) race on it: serialise them.

@@ -16,10 +16,10 @@ PKG = Path(__file__).resolve().parent
 LIB_PATH = PKG / "_build" / "libpagedattn.so"
 
 PA_F16, PA_BF16 = 0, 1
-PA_DEVERR_SLOT, PA_DEVERR_TABLE, PA_DEVERR_LENGTH = 1, 2, 4
+PA_DEVERR_SLOT, PA_DEVERR_TABLE, PA_DEVERR_LENGTH, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
 EXPORTS = ("pa_store_kv", "pa_decode_workspace_size", "pa_decode", "pa_store_decode",
            "pa_store_decode_host", "pa_store_decode_host_workspace_size", "pa_store_decode_host_layout",
-           "pa_prefill_varlen", "pa_decode_noalloc", "pa_status_string", "pa_bm_create",
+           "pa_prefill_varlen", "pa_decode_noalloc", "pa_decode_debug_tail_units", "pa_status_string", "pa_bm_create",
            "pa_bm_destroy", "pa_bm_allocate", "pa_bm_can_allocate", "pa_bm_append",
            "pa_bm_release", "pa_bm_block_table", "pa_bm_num_tokens", "pa_bm_num_free",
            "pa_bm_refcount")
@@ -63,6 +63,8 @@ def load(path: Path | str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_prefill_varlen.restype = I
     lib.pa_decode_noalloc.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, P, P]
     lib.pa_decode_noalloc.restype = I
+    lib.pa_decode_debug_tail_units.argtypes = [P, I, I, I, I, I, I]
+    lib.pa_decode_debug_tail_units.restype = I
     L = ctypes.c_int64
     lib.pa_bm_create.argtypes = [I, I, I]
     lib.pa_bm_create.restype = P
@@ -88,6 +90,14 @@ def load(path: Path | str = LIB_PATH) -> ctypes.CDLL:
     lib.pa_status_string.restype = ctypes.c_char_p
     _lib = lib
     return lib
+
+
+def pa_decode_debug_tail_units(workspace, B: int, Hq: int, Hkv: int, D: int,
+                               max_blocks_per_seq: int, block_size: int) -> int:
+    """Diagnostics: the dynamic-tail units the last completed pa_decode / pa_store_decode launch on
+    this workspace ran (0: equal shares only); -1 on invalid sizes or a failed read."""
+    return int(load().pa_decode_debug_tail_units(_ptr(workspace), int(B), int(Hq), int(Hkv), int(D),
+                                                 int(max_blocks_per_seq), int(block_size)))
 
 
 def status_string(status: int) -> str:

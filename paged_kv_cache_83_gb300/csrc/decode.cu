@@ -1594,6 +1594,20 @@ DecodePlan plan_decode(int B, int Hq, int Hkv, int D, int max_blocks_per_seq, in
     return plan;
 }
 
+int decode_debug_tail_units(const void *workspace, int B, int Hq, int Hkv, int D,
+                            int max_blocks_per_seq, int block_size) {
+    if (!workspace || B < 1 || Hkv < 1 || Hq % Hkv || max_blocks_per_seq < 1 || block_size < 1) return -1;
+    const int G = Hq / Hkv;
+    const size_t P = static_cast<size_t>(device_sm_count()) *
+                     launch_ctas_per_sm(B, Hq, Hkv, D, max_blocks_per_seq, block_size, true);
+    const size_t units = P + tail_units_for(B, Hkv, G, D, max_blocks_per_seq, block_size, P, true);
+    // unit 0 is the static unit of CTA 0, whose record every launch writes
+    SegRecord r{};
+    const char *rec = static_cast<const char *>(workspace) + ws_layout(units, G, D).rec;
+    if (cudaMemcpy(&r, rec, sizeof(r), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+    return r.K2;
+}
+
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream) {
     if (a.B == 0) return cudaSuccess;
     DecodeParams prm{};

@@ -7,6 +7,8 @@
 // one file-scope device array of fixed size, which every GPU that loads this library keeps
 // until the process exits. Everything else is pa_decode itself, called with that array as its
 // workspace.
+#include <atomic>
+
 #include "pa_internal.h"
 
 namespace {
@@ -15,19 +17,23 @@ namespace {
 static __device__ __align__(256) unsigned char g_decode_scratch[PA_DECODE_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_ptr[kMaxDevices] = {nullptr};  // device address of g_decode_scratch, per device
+// device address of g_decode_scratch, per device; host threads may fill a slot concurrently (they
+// all store the same address), so the slots are atomics
+std::atomic<void *> g_scratch_ptr[kMaxDevices];
 
 // The host-side name g_decode_scratch is not a device address; look the address up once per
-// device, with that device current, and keep it.
+// device, with that device current, and keep it. A cudaDeviceReset (or a reset of the primary
+// context) reloads the module, which may move the array: the kept address is then stale, which
+// the header states.
 pa_status scratch_for_current_device(void **ptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
+    void *p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (!p) {
         if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return PA_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
+        g_scratch_ptr[dev].store(p, std::memory_order_release);
     }
-    *ptr = g_scratch_ptr[dev];
+    *ptr = p;
     return PA_OK;
 }
 

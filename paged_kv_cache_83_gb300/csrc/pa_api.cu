@@ -103,6 +103,12 @@ size_t pa_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_blocks_pe
     return pa::plan_decode(B, Hq, Hkv, D, max_blocks_per_seq, block_size).ws_bytes;
 }
 
+int pa_decode_debug_tail_units(const void *workspace, int B, int Hq, int Hkv, int D,
+                               int max_blocks_per_seq, int block_size) {
+    if (pa_decode_workspace_size(B, Hq, Hkv, D, max_blocks_per_seq, block_size) == 0) return -1;
+    return pa::decode_debug_tail_units(workspace, B, Hq, Hkv, D, max_blocks_per_seq, block_size);
+}
+
 }  // extern "C"
 
 namespace pa {

@@ -56,6 +56,10 @@ struct DecodeArgs {
     bool allow_wide = true;                           // see plan_decode
 };
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
+// the dynamic-tail units (K2) of the last completed launch on this workspace (pa_decode's launch
+// configuration), read from unit 0's record; -1 on invalid sizes or a failed copy
+int decode_debug_tail_units(const void *workspace, int B, int Hq, int Hkv, int D,
+                            int max_blocks_per_seq, int block_size);
 // pa_decode with the choice of allow_wide (pa_decode: allowed; pa_decode_noalloc: not, so that
 // its fixed scratch covers the same shapes whatever the batch)
 pa_status decode_entry(void *out, const void *q, const void *k_cache, const void *v_cache,

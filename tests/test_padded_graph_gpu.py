@@ -115,7 +115,7 @@ def test_graph_replays_with_and_without_the_dynamic_tail(orc):
     with torch.cuda.graph(g):
         body()
     # full batches of long contexts (about 14 k tiles: the tail runs), then a small batch (equal
-    # shares), then full batches again
+    # shares), then full batches again; each replay's choice is read back from the workspace
     for n_real, seed, lo in [(bucket, 12, 700), (16, 13, 1), (bucket, 14, 700), (bucket, 15, 900),
                              (8, 16, 1), (bucket, 12, 700)]:
         c = batch(n_real, seed, lo)
@@ -128,6 +128,9 @@ def test_graph_replays_with_and_without_the_dynamic_tail(orc):
         g.replay()
         torch.cuda.synchronize()
         assert int(err.item()) == 0
+        # the replay took the path it was meant to exercise: the kernel's own choice, read back
+        tail = pa.pa_decode_debug_tail_units(ws, bucket, Hq, Hkv, D, maxb, bs)
+        assert (tail > 0) if n_real == bucket else (tail == 0), (n_real, tail)
         kref, vref = orc.store_kv(c.k_new, c.v_new, c.k_cache, c.v_cache, c.slot_mapping)
         assert np.array_equal(bits(bufs["kc"]), kref) and np.array_equal(bits(bufs["vc"]), vref)
         o = f64(out)

@@ -2,7 +2,7 @@
 
 Covers the pool path (prefix cached, block table given, new rows stored first) and the packed
 path (no table), causal and not, ragged prompt lengths around the 64/128-row tiles, both
-dtypes, D 64/128 and several group sizes; the full prefill_prefix workload on sampled prompts.
+dtypes, D 64/128 and several group sizes; every row of the full prefill_prefix workload.
 """
 import numpy as np
 import pytest
@@ -132,17 +132,35 @@ def test_empty_is_noop():
     torch.cuda.synchronize()
 
 
-def test_full_prefill_workload_sampled(orc):
+@pytest.fixture(scope="module")
+def full_prefill(orc):
+    """The prefill_prefix workload (64 prompts, 512-token shared prefix) in the launch
+    configuration the bench times: store, then prefill, once on the GPU; the oracle's own scatter
+    gives the pools its reference attends over."""
     c = W.make("prefill_prefix")
     out, kc, vc, err = _run_pool(c)
-    assert int(err.item()) == 0
-    o = f64(out)
+    kref, vref = orc.store_kv(c.k, c.v, c.k_cache, c.v_cache, c.slot_mapping)
+    return c, f64(out), bits(kc), bits(vc), int(err.item()), kref, vref
+
+
+def test_full_prefill_workload_store_and_errors(full_prefill):
+    c, o, kc, vc, err, kref, vref = full_prefill
+    assert err == 0
+    assert np.array_equal(kc, kref) and np.array_equal(vc, vref)
     assert np.isfinite(o).all()
-    ql = c.q_lens
-    seqs = sorted({int(np.argmin(ql)), int(np.argmax(ql)), 5, 33})
-    refs, kref, vref = _ref_pool(orc, c, seqs=seqs)
-    assert np.array_equal(bits(kc), kref) and np.array_equal(bits(vc), vref)
-    for s, ref in zip(seqs, refs):
-        a, b = c.cu_seqlens_q[s], c.cu_seqlens_q[s + 1]
-        e = max_abs(o[a:b], ref)
-        assert e <= TOL["bf16"], (s, e)
+
+
+@pytest.mark.parametrize("part", range(4))
+def test_full_prefill_workload_every_prompt(orc, full_prefill, part):
+    """Every output row of all 64 prompts against the fp64 oracle, a quarter of the prompts per
+    case (the work items go out largest first across the whole launch, so any prompt may be
+    split over several CTAs)."""
+    c, o, _, _, _, kref, vref = full_prefill
+    s0, s1 = 16 * part, 16 * (part + 1)
+    a, b = int(c.cu_seqlens_q[s0]), int(c.cu_seqlens_q[s1])
+    ka = int(c.cu_seqlens_k[s0])
+    ref = orc.prefill(c.q[a:b], None, None, kref, vref, c.cu_seqlens_q[s0:s1 + 1] - a,
+                      c.cu_seqlens_k[s0:s1 + 1] - ka, c.block_tables[s0:s1], Hkv=c.Hkv,
+                      block_size=c.block_size, scale=c.scale, dtype=c.dtype)
+    e = max_abs(o[a:b], ref)
+    assert e <= TOL["bf16"], e

@@ -1,16 +1,20 @@
-"""pa_decode_noalloc against pa_decode, through the C ABI, on the GPU.
+"""pa_decode_noalloc through the C ABI on the GPU, against the fp64 oracle and against pa_decode.
 
 pa_decode_noalloc serves callers that cannot allocate device memory (a host framework that owns
 every allocation, a process whose device memory is already reserved, a step loop that cannot
 afford cudaMalloc's synchronisation): its split-K scratch is a fixed device array inside the
-library. This file is named so that pytest collects it last.
+library. Its launch differs from pa_decode's (one unit per CTA, no units handed out as CTAs
+finish), so it is checked against the oracle itself, on two calls in a row that share the array.
+This file is named so that pytest collects it last.
 """
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_83_gb300 as pa
 import workloads as W
-from tests.gpu_util import TOL, DecodeRun, f64, max_abs
+from tests.gpu_util import TOL, DecodeRun, bits, f64, max_abs
 
 pytestmark = pytest.mark.gpu
 
@@ -20,7 +24,8 @@ def _case(seed):
     return W.make("qwen3_06b_decode", seed=seed, n=24)
 
 
-def test_noalloc_matches_decode_on_two_calls_in_a_row():
+def test_noalloc_matches_oracle_and_decode_on_two_calls_in_a_row():
+    orc = oracle.get()
     for seed in (101, 202):
         c = _case(seed)
         # pa_decode's own workspace also holds the units of its dynamic tail; the no-alloc entry
@@ -29,11 +34,16 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row():
         assert need > 0
         run = DecodeRun(c)
         ref = run.step().clone()                 # store + pa_decode with a caller workspace
+        kref, vref = orc.store_kv(c.k_new, c.v_new, c.k_cache, c.v_cache, c.slot_mapping)
+        assert np.array_equal(bits(run.kc), kref) and np.array_equal(bits(run.vc), vref)
+        exact = orc.decode(c.q, kref, vref, c.block_tables, c.context_lens, scale=c.scale,
+                           dtype=c.dtype)
         out = torch.full_like(run.q, float("nan"))
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         pa.pa_decode_noalloc(out, run.q, run.kc, run.vc, run.bt, run.cl, c.scale, err=err)
         torch.cuda.synchronize()
         assert int(err.item()) == 0
+        assert max_abs(f64(out), exact) <= TOL[c.dtype]
         assert max_abs(f64(out), f64(ref)) <= TOL[c.dtype]
 
 

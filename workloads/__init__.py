@@ -36,7 +36,7 @@ import numpy as np
 
 __all__ = [
     "DecodeCase", "PrefillCase", "BlockAllocator", "CONFIGS", "normal_bits",
-    "decode_case", "prefill_case", "make",
+    "decode_case", "prefill_case", "make", "lengths",
 ]
 
 F16, BF16 = "f16", "bf16"
@@ -396,6 +396,12 @@ def _lengths(name: str, seed: int, n: int | None = None) -> np.ndarray:
         x = rng.lognormal(mean=math.log(2048.0), sigma=1.0, size=n or 512)
         return np.clip(np.rint(x), 1, 16384).astype(np.int64)
     raise KeyError(name)
+
+
+def lengths(name: str, seed: int | None = None, n: int | None = None) -> np.ndarray:
+    """The per-sequence lengths (contexts, or prompt lengths) of a named workload, without
+    building its pools: what ``make(name, seed, n)`` would use."""
+    return _lengths(name, CONFIGS[name].seed if seed is None else seed, n)
 
 
 def make(name: str, seed: int | None = None, n: int | None = None):
