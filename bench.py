@@ -19,7 +19,8 @@ steps per second per layer. The same line carries:
   host's cores;
 * ``rows``: the other rows of the path measured the same way: the same step as two calls
   (pa_store_kv, then pa_decode), the store alone, the varlen prefill with a 512-token cached
-  prefix (``prefill_prefix``) with its store, and the two small decode workloads as CUDA graphs.
+  prefix (``prefill_prefix``) with its store, the same prefill at the Qwen2.5-0.5B head shape
+  (``qwen25_prefill``: 14/2 heads, head dim 64), and the two small decode workloads as CUDA graphs.
 
 ``--impl reference`` times the CPU oracle as the reference arm, on the same metric.
 Multi-GPU (torchrun): every rank runs an independent replica (the path shards by sequence
@@ -52,14 +53,16 @@ DEFAULT_WORKLOAD = "qwen3_06b_decode"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM traffic (read + write bytes) of one launch, from the ncu captures of these kernels (layer 0
-# of the default workload; prefill_prefix). Each is valid only for the kernel sources it was taken
+# of the default workload; prefill_prefix; qwen25_prefill). Each is valid only for the kernel sources it was taken
 # on, identified by their hash; after any change the bench reports null.
 DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_289_356_032,
                   "sha256": "1361a7dda18d1b40a99411ced40578b9055708f5be1b9b61207b8c3b496cd270"}
 STORE_TRAFFIC = {"sources": ("store_kv.cu", "pa_common.cuh"), "bytes": 218_096_128,
                  "sha256": "9940671f5a00740d1ba3ee485ac0d8bdb7dee7db79bbd1fe95feb25da0dc412c"}
-PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 699_134_976,
-                   "sha256": "bc2aa36307645f2b743031ee20edb4d4d1480634c459f3d96973e9c06ba665b3"}
+PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 419_378_688,
+                   "sha256": "023bbfe2d5a20ef6c1d50b49eb051c8631f5d26adf21a7c73bd298741d2960a6"}
+PREFILL_QWEN25_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 111_387_648,
+                          "sha256": "023bbfe2d5a20ef6c1d50b49eb051c8631f5d26adf21a7c73bd298741d2960a6"}
 
 
 def peaks() -> tuple[dict, str]:
@@ -329,7 +332,7 @@ def run_gpu(args, ws_, rank, local):
     bf16_sustained = float(pk.get("bf16_tflops_sustained", bf16_peak))
 
     if args.only == "prefill":
-        # the prefill row alone (store + varlen prefill on prefill_prefix): a short command for
+        # the prefill rows alone (store + varlen prefill on the two prefill workloads): a short command for
         # profiling those two kernels without the decode pools on the device
         rows = bench_prefill(torch, pa, dev, stream, bf16_peak, bf16_sustained, hbm, args, pk_kind)
         if rank == 0:
@@ -728,8 +731,10 @@ def bench_block_manager(pa) -> dict:
     return out
 
 
-def bench_prefill(torch, pa, dev, stream, bf16_peak, bf16_sustained, hbm, args, pk_kind) -> dict:
-    c = W.make("prefill_prefix")
+def time_prefill(torch, pa, dev, stream, name, steps):
+    """Store + varlen prefill of one prefill workload, L2 flushed before each iteration: the mean
+    CUDA-event times (ms) of the store and of the prefill, and the case."""
+    c = W.make(name)
     i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
     kc, vc = to_dev(torch, c.k_cache, c.dtype, dev), to_dev(torch, c.v_cache, c.dtype, dev)
     k, v, q = (to_dev(torch, x, c.dtype, dev) for x in (c.k, c.v, c.q))
@@ -752,7 +757,7 @@ def bench_prefill(torch, pa, dev, stream, bf16_peak, bf16_sustained, hbm, args, 
 
     for _ in range(3):
         run()
-    n = max(3, min(args.steps, 50))
+    n = max(3, min(steps, 50))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
     torch.cuda.synchronize()
     for e in evs:
@@ -761,22 +766,33 @@ def bench_prefill(torch, pa, dev, stream, bf16_peak, bf16_sustained, hbm, args, 
     torch.cuda.synchronize()
     st = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     pf = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    flops = prefill_flops(c.q_lens, c.k_lens, c.Hq, c.D)
-    st_bytes = 4 * int(c.q.shape[0]) * c.Hkv * c.D * 2
-    return {"prefill": {"workload": "prefill_prefix", "kernel": "prefill_tc_kernel",
-                        "ms": pf, "TFLOP_per_s": flops / (pf * 1e-3) / 1e12,
-                        "frac_of_bf16_peak": flops / (pf * 1e-3) / 1e12 / bf16_peak,
-                        "peak": bf16_peak, "peak_source": f"{pk_kind} bf16_tflops (burst: the "
-                                                          f"kernel is timed alone)",
-                        "frac_of_bf16_sustained": flops / (pf * 1e-3) / 1e12 / bf16_sustained,
-                        "flops": flops, "l2": "flushed between iterations (a 256 MB read sweep)",
-                        "traffic": traffic_of(PREFILL_TRAFFIC)},
-            "store_kv_prefill": {"kernel": "store_kv_kernel", "ms": st, "bytes": st_bytes,
-                                 "GB_per_s": st_bytes / (st * 1e-3) / 1e9,
-                                 "frac_of_hbm": st_bytes / (st * 1e-3) / 1e9 / hbm,
-                                 "traffic": traffic_of(STORE_TRAFFIC),
-                                 "traffic_note": "ncu DRAM read + write of one launch; part of the "
-                                                 "writes are still in L2 when it ends"}}
+    return st, pf, c
+
+
+def bench_prefill(torch, pa, dev, stream, bf16_peak, bf16_sustained, hbm, args, pk_kind) -> dict:
+    rows = {}
+    for name, row, traffic in (("prefill_prefix", "prefill", PREFILL_TRAFFIC),
+                               ("qwen25_prefill", "prefill_qwen25", PREFILL_QWEN25_TRAFFIC)):
+        st, pf, c = time_prefill(torch, pa, dev, stream, name, args.steps)
+        flops = prefill_flops(c.q_lens, c.k_lens, c.Hq, c.D)
+        rows[row] = {"workload": name, "kernel": "prefill_tc_kernel",
+                     "Hq": c.Hq, "Hkv": c.Hkv, "D": c.D, "block_size": c.block_size, "dtype": c.dtype,
+                     "ms": pf, "TFLOP_per_s": flops / (pf * 1e-3) / 1e12,
+                     "frac_of_bf16_peak": flops / (pf * 1e-3) / 1e12 / bf16_peak,
+                     "peak": bf16_peak, "peak_source": f"{pk_kind} bf16_tflops (burst: the "
+                                                       f"kernel is timed alone)",
+                     "frac_of_bf16_sustained": flops / (pf * 1e-3) / 1e12 / bf16_sustained,
+                     "flops": flops, "l2": "flushed between iterations (a 256 MB read sweep)",
+                     "traffic": traffic_of(traffic)}
+        if name == "prefill_prefix":
+            st_bytes = 4 * int(c.q.shape[0]) * c.Hkv * c.D * 2
+            rows["store_kv_prefill"] = {"kernel": "store_kv_kernel", "ms": st, "bytes": st_bytes,
+                                        "GB_per_s": st_bytes / (st * 1e-3) / 1e9,
+                                        "frac_of_hbm": st_bytes / (st * 1e-3) / 1e9 / hbm,
+                                        "traffic": traffic_of(STORE_TRAFFIC),
+                                        "traffic_note": "ncu DRAM read + write of one launch; part of "
+                                                        "the writes are still in L2 when it ends"}
+    return rows
 
 
 def main():

@@ -243,8 +243,9 @@ pa_status pa_store_decode_host(void *out_host, const void *q_host, const void *k
  * total_q       host int: rows of q and out (= cu_seqlens_q[S]); bounds every read of q.
  * total_k       host int: rows of the packed k, v (= cu_seqlens_k[S]) when block_tables is NULL;
  *               ignored otherwise.
- * max_seqlen_q  host int >= every q_len (sizes the grid); max_seqlen_k is accepted for
- *               interface parity and not needed.
+ * max_seqlen_q  host int >= every q_len (sizes the grid).
+ * max_seqlen_k  host int, a bound on k_len used only to order the work (how many prompts run
+ *               together so that their keys stay in L2); any value gives the same result.
  * S == 0 is a no-op.
  */
 pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void *v,

@@ -271,7 +271,6 @@ pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void 
                             const int32_t *block_tables, int max_blocks_per_seq, int Hq, int Hkv,
                             int D, int block_size, int num_blocks, float scale, int causal,
                             pa_dtype dtype, int32_t *err, cudaStream_t stream) {
-    (void)max_seqlen_k;
     if (!dtype_ok(dtype)) return PA_ERR_DTYPE;
     if (S < 0 || max_seqlen_q < 0 || total_q < 0 || (!block_tables && total_k < 0) ||
         (causal != 0 && causal != 1))
@@ -306,6 +305,7 @@ pa_status pa_prefill_varlen(void *out, const void *q, const void *k, const void 
     a.total_q = total_q;
     a.total_k = block_tables ? 0 : total_k;
     a.max_seqlen_q = max_seqlen_q;
+    a.max_seqlen_k = max_seqlen_k;  // a hint for the work order only
     a.max_blocks = max_blocks_per_seq;
     a.Hq = Hq;
     a.Hkv = Hkv;

@@ -74,13 +74,14 @@ struct PrefillArgs {
     const void *q, *k, *v, *k_cache, *v_cache;
     const int32_t *cu_q, *cu_k, *block_tables;
     int S, max_seqlen_q, max_blocks, Hq, Hkv, D, block_size, num_blocks, causal;
+    int max_seqlen_k;      // the caller's bound on keys per sequence: orders the work, nothing else
     int total_q, total_k;  // rows of q / out, and of the packed k, v
     float scale;
     pa_dtype dtype;
     int32_t *err;
 };
 cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t stream);
-// tensor-core (tcgen05) prefill: head dim 128, even group size, K/V boxes of >= 8 rows
+// tensor-core (tcgen05) prefill: head dim 64 or 128, any group size, K/V boxes of >= 8 rows
 bool tc_prefill_supported(const PrefillArgs &a);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
 

@@ -1,6 +1,7 @@
 // prefill_mma.cu: varlen causal prefill with a paged prefix (pa_prefill_varlen), warp-level
-// mma.sync version: the general path for the shapes the tcgen05 kernel (prefill_tc.cu) does not
-// take (head dim 64, odd group sizes, block sizes without an 8-row power-of-two divisor).
+// mma.sync version: the general path for the launches the tcgen05 kernel (prefill_tc.cu) does not
+// take (pool block sizes without an 8-row power-of-two divisor, an output that is not 16-byte
+// aligned).
 //
 // Source: "nano-vLLM Part 4", section 3 (prefill: packed prompts, variable-length attention with
 // an optional prefix block table); smzdm nano-vLLM deep dive, "GPU执行优化" (cu_seqlens mark the

@@ -6,9 +6,11 @@
 // boundaries) and "模型实现细节" (prefix cache used when cu_seqlens_k > cu_seqlens_q); "mini-vLLM"
 // (prompts attending causally to themselves).
 //
-// Persistent: one CTA per SM takes work items (128 query rows of one sequence for the two query
-// heads of a GQA pair, which share every K/V tile) from a counter until none is left, so the
-// start-up of one item overlaps the end of the previous one. Shapes: head dim 128, even groups.
+// Persistent: one CTA per SM takes work items (128 query rows of one sequence for two query heads
+// of one GQA group, which share every K/V tile) from a counter until none is left, so the start-up
+// of one item overlaps the end of the previous one. Head dim 64 or 128 (one or two 64-column halves
+// per tile); a group of G query heads is cut into ceil(G / 2) pairs, and the pair that has one head
+// (odd G) computes its second head on a zero Q tile whose output is dropped.
 //
 //   warp 3      scheduler: claims items, reads their lengths, checks the block table, drops items
 //               without rows, writes zero rows + an error bit for bad ones, and queues the rest.
@@ -34,6 +36,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "pa_internal.h"
@@ -42,14 +45,11 @@ namespace pa {
 
 namespace {
 
-constexpr int BM = 128, BN = 128, HD = 128;
+constexpr int BM = 128, BN = 128;
 constexpr int kThreads = 384;
 constexpr int kHalf = BM * 64 * 2;  // one 128-row x 64-column half tile: 16 KB
-constexpr int kTile = 2 * kHalf;    // 128 x 128 elements: 32 KB
+constexpr int kPTile = BM * BN * 2; // P (128 rows x 128 keys): 32 KB, also the output stage
 constexpr int kRing = 3;            // K/V tile slots
-constexpr uint32_t kTileDesc = kTile >> 4;  // one tile further, in descriptor address units
-constexpr int OFF_QA = 0, OFF_QB = kTile, OFF_PA = 2 * kTile, OFF_PB = 3 * kTile, OFF_RING = 4 * kTile,
-              OFF_BAR = OFF_RING + kRing * kTile;
 // per-head barriers take index base + h (h = 0 for head A, 1 for head B)
 enum {
     B_QFULL = 0,               // the item's two Q tiles landed (TMA transaction count)
@@ -69,15 +69,25 @@ enum {
 };
 constexpr int kItemReaders = 11;  // producer, two MMA issuers, eight softmax warps
 
-// One work item: 128 query rows of sequence s for the query heads 2 pair, 2 pair + 1.
-// nkv == 0 marks the end of the work.
+// One work item: 128 query rows of sequence s for the query heads ha and hb (hb < 0: the pair has
+// one head) of the GQA group of kv head g. nkv == 0 marks the end of the work.
 struct ItemInfo {
-    int s, q0, k0, kl, m0, mrows, P, n_end, nkv, pair, pad0, pad1;
+    int s, q0, k0, kl, m0, mrows, P, n_end, nkv, ha, hb, g;
 };
-constexpr int OFF_ITEMS = OFF_BAR + NBAR * 8;
-constexpr int OFF_MISC = OFF_ITEMS + 2 * static_cast<int>(sizeof(ItemInfo));  // tmem base, abort flag
-constexpr int kSmem = OFF_MISC + 16 + 1024;                                   // + alignment slack
-static_assert(kSmem <= 232448, "shared memory per CTA");
+// shared-memory layout for head dim HD: Q tiles, P tiles, the K/V ring, barriers, the item queue
+template <int HD>
+struct TcLayout {
+    static constexpr int kHalves = HD / 64;    // 64-column halves per tile row
+    static constexpr int kQ = BM * HD * 2;     // one Q tile
+    static constexpr int kKV = BN * HD * 2;    // one K or V tile
+    static constexpr uint32_t kKVDesc = kKV >> 4;  // one ring slot further, in descriptor units
+    static constexpr int OFF_QA = 0, OFF_QB = kQ, OFF_PA = 2 * kQ, OFF_PB = OFF_PA + kPTile,
+                         OFF_RING = OFF_PB + kPTile, OFF_BAR = OFF_RING + kRing * kKV;
+    static constexpr int OFF_ITEMS = OFF_BAR + NBAR * 8;
+    static constexpr int OFF_MISC = OFF_ITEMS + 2 * static_cast<int>(sizeof(ItemInfo));  // tmem base, abort flag
+    static constexpr int kSmem = OFF_MISC + 16 + 1024;                                   // + alignment slack
+    static_assert(kSmem <= 232448, "shared memory per CTA");
+};
 constexpr unsigned kFull = 0xffffffffu;
 
 struct TcParams {
@@ -86,8 +96,10 @@ struct TcParams {
     void *out;
     int32_t *err;
     unsigned long long *sched;  // [0]: next work item, [1]: CTAs finished (both 0 between launches)
-    long long n_items;          // S * pairs * row blocks
-    int S, Hq, Hkv, G, max_blocks, num_blocks, causal, max_seqlen_q, box_rows, row_blocks, pairs;
+    long long n_items;          // bands * band * pairs * row blocks
+    int S, Hq, Hkv, G, max_blocks, num_blocks, causal, max_seqlen_q, box_rows, row_blocks;
+    int pairs;                  // Hkv * ceil(G / 2)
+    int band;                   // prompts per band of the item order
     BlockGeom geom;
     float scale_log2;
 };
@@ -110,9 +122,14 @@ __device__ __forceinline__ void tc_abort(int32_t *err, volatile int *abort_flag)
 // the next tile's QK is issued before the current tile's PV, across item boundaries too:
 //   K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), K0', V(n-1), K1', V0', ...
 // Load i uses slot i % kRing; the producer and both MMA issuers count loads the same way.
-template <class E>
+template <class E, int HD>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcParams p) {
     using T = typename E::T;
+    using Lay = TcLayout<HD>;
+    constexpr int OFF_QA = Lay::OFF_QA, OFF_QB = Lay::OFF_QB, OFF_PA = Lay::OFF_PA, OFF_PB = Lay::OFF_PB,
+                  OFF_RING = Lay::OFF_RING, OFF_BAR = Lay::OFF_BAR, OFF_ITEMS = Lay::OFF_ITEMS,
+                  OFF_MISC = Lay::OFF_MISC;
+    constexpr int kHalves = Lay::kHalves;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_addr(smem);
@@ -161,14 +178,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const long long idx = static_cast<long long>(__shfl_sync(kFull, nxt, 0));
             if (idx >= p.n_items) break;
             if (lane == 0) nxt = atomicAdd(p.sched, 1ull);  // in flight while this one is resolved
-            // tickets by rank r of a row block counted from its prompt's last one (the block with
-            // the most keys), then prompt, then pair: large items first across the whole launch,
-            // and the last ones handed out are the first row blocks of long prompts, the smallest
-            const long long per_rank = static_cast<long long>(p.S) * p.pairs;
-            const int r = static_cast<int>(idx / per_rank);
-            const int rem = static_cast<int>(idx % per_rank);
-            const int s = rem / p.pairs;
+            // tickets by band of p.band prompts, then rank r of a row block counted from its
+            // prompt's last one (the block with the most keys), then prompt, then pair: within a
+            // band large items go first and the last ones are the first row blocks of long prompts,
+            // the smallest; a band's K/V stays in L2 while its row blocks run
+            const long long per_rank = static_cast<long long>(p.band) * p.pairs;
+            const long long per_band = per_rank * p.row_blocks;
+            const int bnd = static_cast<int>(idx / per_band);
+            const long long rem0 = idx % per_band;
+            const int r = static_cast<int>(rem0 / per_rank);
+            const int rem = static_cast<int>(rem0 % per_rank);
+            const int s = bnd * p.band + rem / p.pairs;
             const int pair = rem % p.pairs;
+            if (s >= p.S) continue;
+            // the pair's query heads: pairs of one group's heads, the last one alone for odd G
+            const int ppg = (p.G + 1) / 2;
+            const int g = pair / ppg, hk = 2 * (pair % ppg);
+            const int ha = g * p.G + hk, hb = hk + 1 < p.G ? ha + 1 : -1;
             const int q0 = p.cu_q[s], ql = p.cu_q[s + 1] - q0;
             const int k0 = p.cu_k[s], kl = p.cu_k[s + 1] - k0;
             if (ql < 0 || ql > p.max_seqlen_q) {
@@ -199,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 if (lane == 0) raise_err(p.err, bad ? PA_DEVERR_LENGTH : PA_DEVERR_TABLE);
                 for (int i = lane; i < mrows * HD * 2; i += 32) {
                     const int r = i / (2 * HD), h = (i / HD) & 1, d = i % HD;
-                    out[(static_cast<size_t>(q0 + m0 + r) * p.Hq + 2 * pair + h) * HD + d] = T(0.f);
+                    const int head = h ? hb : ha;
+                    if (head >= 0) out[(static_cast<size_t>(q0 + m0 + r) * p.Hq + head) * HD + d] = T(0.f);
                 }
                 continue;
             }
@@ -208,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             if (lane == 0) {
                 ItemInfo it;
                 it.s = s, it.q0 = q0, it.k0 = k0, it.kl = kl, it.m0 = m0, it.mrows = mrows, it.P = P;
-                it.n_end = n_end, it.nkv = (n_end + BN - 1) / BN, it.pair = pair, it.pad0 = it.pad1 = 0;
+                it.n_end = n_end, it.nkv = (n_end + BN - 1) / BN, it.ha = ha, it.hb = hb, it.g = g;
                 items[published & 1] = it;
                 mbar_arrive(bar(B_IFULL + (published & 1)));  // release: the entry is visible
             }
@@ -246,17 +273,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 row = trow ? trow[p.geom.block_of(pos)] * p.geom.block_size + p.geom.offset_of(pos)
                            : it.k0 + pos;
             }
-            const uint32_t bytes = __popc(__ballot_sync(kFull, row >= 0)) * box_bytes * 2;
+            const uint32_t bytes = __popc(__ballot_sync(kFull, row >= 0)) * box_bytes * kHalves;
             const int slot = static_cast<int>(L % kRing);
             if (!tc_warp_wait(bar(B_EMPTY + slot), static_cast<uint32_t>((L / kRing) & 1) ^ 1, abort_flag))
                 return false;
             if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL + slot), bytes);
             __syncwarp();
             if (row >= 0) {
-                const uint32_t dst = sbase + OFF_RING + slot * kTile + lane * R * 128;
-                const int g = 2 * it.pair / p.G;
-                for (int half = 0; half < 2; ++half)
-                    tma_load_3d(dst + half * kHalf, is_v ? &p.tm_v : &p.tm_k, half * 64, g, row,
+                const uint32_t dst = sbase + OFF_RING + slot * Lay::kKV + lane * R * 128;
+                for (int half = 0; half < kHalves; ++half)
+                    tma_load_3d(dst + half * kHalf, is_v ? &p.tm_v : &p.tm_k, half * 64, it.g, row,
                                 bar(B_FULL + slot));
             }
             ++L;
@@ -272,11 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             if (ok && n > 0) ok = tc_warp_wait(bar(B_QEMPTY), (n - 1) & 1, abort_flag);
             if (!ok) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(bar(B_QFULL), 2 * kTile);
+                mbar_arrive_expect_tx(bar(B_QFULL), 2 * Lay::kQ);
+                // a missing second head reads past the last head: the tile is zero-filled
                 for (int h = 0; h < 2; ++h)
-                    for (int half = 0; half < 2; ++half)
+                    for (int half = 0; half < kHalves; ++half)
                         tma_load_3d(sbase + (h ? OFF_QB : OFF_QA) + half * kHalf, &p.tm_q, half * 64,
-                                    2 * cur.pair + h, cur.q0 + cur.m0, bar(B_QFULL));
+                                    h ? (cur.hb >= 0 ? cur.hb : p.Hq) : cur.ha, cur.q0 + cur.m0,
+                                    bar(B_QFULL));
             }
             __syncwarp();
             for (int j = 1; ok && j < cur.nkv; ++j)
@@ -308,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const uint64_t dv0 = smem_desc_sw128(sbase + OFF_RING, kHalf, 1024);
         const uint32_t s_tm = tmem + (h ? 128 : 0), o_tm = tmem + 256 + (h ? 128 : 0);
         auto qk = [&](int slot) {  // S = Q K^T: A = Q (K-major), B = K rows (K-major)
-            const uint64_t kb = dk0 + slot * kTileDesc;
+            const uint64_t kb = dk0 + slot * Lay::kKVDesc;
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
@@ -316,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             }
         };
         auto pv = [&](int slot, bool acc) {  // O += P V: A = P (K-major), B = V rows (N-major)
-            const uint64_t vb = dv0 + slot * kTileDesc;
+            const uint64_t vb = dv0 + slot * Lay::kKVDesc;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
@@ -383,9 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 // The last tile may hold rows past the keys (unwritten slots or another prompt):
                 // zero them before any PV reads them (P is zero there, but 0 * NaN is not).
                 if (h == 0) {
-                    unsigned char *vt = smem + OFF_RING + slot * kTile;
-                    for (int c = lane; c < (BN - last_valid) * 16; c += 32) {  // 16-byte chunks
-                        const int r = last_valid + c / 16, c16 = c % 16;
+                    unsigned char *vt = smem + OFF_RING + slot * Lay::kKV;
+                    for (int c = lane; c < (BN - last_valid) * (HD / 8); c += 32) {  // 16-byte chunks
+                        const int r = last_valid + c / (HD / 8), c16 = c % (HD / 8);
                         *reinterpret_cast<uint4 *>(vt + (c16 >> 3) * kHalf + r * 128 + (c16 & 7) * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
@@ -502,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 // O(t - 1) is complete: rescale it before this tile's PV adds to it
                 if (j > 0 && __any_sync(kFull, need)) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < HD / 32; ++c) {
                         uint32_t ov[32];
                         tmem_ld32(orow + c * 32, ov);
                         tmem_wait_ld();
@@ -521,9 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             if (!ok) break;
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint32_t ov[64];  // the output row, packed
+            uint32_t ov[HD / 2];  // the output row, packed
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < HD / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32(orow + c * 32, v);
                 tmem_wait_ld();
@@ -538,30 +566,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             // The warp's 32 rows go out through their own rows of the P buffer (swizzled like P):
             // two TMA stores when all 32 rows belong to the item, else row-wide 16-byte stores.
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
+            for (int c = 0; c < HD / 8; ++c)
                 *reinterpret_cast<uint4 *>(prow + (c >> 3) * kHalf + (((c & 7) ^ (r & 7)) << 4)) =
                     make_uint4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
             const unsigned char *pw = smem + (h ? OFF_PB : OFF_PA);
-            if (quarter * 32 + 32 <= it.mrows) {
+            const int head = h ? it.hb : it.ha;  // < 0: this pair has no second head
+            if (head < 0) {
+                __syncwarp();
+            } else if (quarter * 32 + 32 <= it.mrows) {
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     const int row0 = it.q0 + it.m0 + quarter * 32;
-                    for (int half = 0; half < 2; ++half)
-                        tma_store_3d(&p.tm_o, half * 64, 2 * it.pair + h, row0,
+                    for (int half = 0; half < kHalves; ++half)
+                        tma_store_3d(&p.tm_o, half * 64, head, row0,
                                      smem_addr(pw + half * kHalf + quarter * 32 * 128));
                     bulk_commit();
                 }
             } else {
                 __syncwarp();
 #pragma unroll 4
-                for (int i = 0; i < 16; ++i) {
-                    const int k = i * 32 + lane, rr = quarter * 32 + (k >> 4), c = k & 15;
+                for (int i = 0; i < HD / 8; ++i) {  // 32 rows x HD / 8 chunks of 16 bytes
+                    const int k = i * 32 + lane, rr = quarter * 32 + k / (HD / 8), c = k % (HD / 8);
                     const uint4 u = *reinterpret_cast<const uint4 *>(pw + (c >> 3) * kHalf + rr * 128 +
                                                                      (((c & 7) ^ (rr & 7)) << 4));
                     if (rr < it.mrows)
                         *reinterpret_cast<uint4 *>(out + (static_cast<size_t>(it.q0 + it.m0 + rr) * p.Hq +
-                                                          2 * it.pair + h) * HD + c * 8) = u;
+                                                          head) * HD + c * 8) = u;
                 }
             }
             __syncwarp();  // the rows are read before the next tile's P overwrites them
@@ -601,12 +632,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn_tc() {
     return fn;
 }
 
-// [rows, heads, 128] tensor, box [box_rows, 1, 64], 128-byte swizzle
-bool encode_rows(CUtensorMap *m, const void *base, pa_dtype dt, int heads, long long rows, int box_rows) {
+// [rows, heads, hd] tensor, box [box_rows, 1, 64], 128-byte swizzle
+bool encode_rows(CUtensorMap *m, const void *base, pa_dtype dt, int heads, int hd, long long rows, int box_rows) {
     auto fn = encode_fn_tc();
     if (!fn || rows <= 0) return false;
-    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(heads) * 256};
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(hd), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(hd) * 2, static_cast<cuuint64_t>(heads) * hd * 2};
     cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
@@ -634,9 +665,10 @@ unsigned long long *sched_slot() {
     return base[dev] + 2 * (next.fetch_add(1u) % kSchedSlots);
 }
 
-template <class E>
+template <class E, int HD>
 cudaError_t launch_tc_typed(const TcParams &prm, cudaStream_t stream) {
-    auto kern = prefill_tc_kernel<E>;
+    auto kern = prefill_tc_kernel<E, HD>;
+    constexpr int kSmem = TcLayout<HD>::kSmem;
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -665,7 +697,7 @@ int tc_box_rows(const PrefillArgs &a) {
 bool tc_prefill_supported(const PrefillArgs &a) {
     // the output rows leave through TMA stores and 16-byte stores
     const bool out_aligned = (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
-    return a.D == 128 && (a.Hq / a.Hkv) % 2 == 0 && tc_box_rows(a) >= 8 && a.total_q > 0 &&
+    return (a.D == 64 || a.D == 128) && tc_box_rows(a) >= 8 && a.total_q > 0 &&
            (a.block_tables ? true : a.total_k > 0) && out_aligned;
 }
 
@@ -676,10 +708,10 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     const void *vb = a.block_tables ? a.v_cache : a.v;
     const long long krows = a.block_tables ? static_cast<long long>(a.num_blocks) * a.block_size
                                            : static_cast<long long>(a.total_k);
-    if (!encode_rows(&prm.tm_q, a.q, a.dtype, a.Hq, a.total_q, 128) ||
-        !encode_rows(&prm.tm_k, kb, a.dtype, a.Hkv, krows, R) ||
-        !encode_rows(&prm.tm_v, vb, a.dtype, a.Hkv, krows, R) ||
-        !encode_rows(&prm.tm_o, a.out, a.dtype, a.Hq, a.total_q, 32))
+    if (!encode_rows(&prm.tm_q, a.q, a.dtype, a.Hq, a.D, a.total_q, 128) ||
+        !encode_rows(&prm.tm_k, kb, a.dtype, a.Hkv, a.D, krows, R) ||
+        !encode_rows(&prm.tm_v, vb, a.dtype, a.Hkv, a.D, krows, R) ||
+        !encode_rows(&prm.tm_o, a.out, a.dtype, a.Hq, a.D, a.total_q, 32))
         return cudaErrorInvalidValue;
     prm.cu_q = a.cu_q;
     prm.cu_k = a.cu_k;
@@ -696,14 +728,20 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     prm.max_seqlen_q = a.max_seqlen_q;
     prm.box_rows = R;
     prm.row_blocks = (a.max_seqlen_q + BM - 1) / BM;
-    prm.pairs = a.Hq / 2;
-    prm.n_items = static_cast<long long>(prm.row_blocks) * prm.pairs * a.S;
+    prm.pairs = a.Hkv * ((prm.G + 1) / 2);
+    // prompts per band: the K/V of a band (at most max_seqlen_k keys a prompt) within 64 MB of L2
+    const double kv_bytes = static_cast<double>(a.max_seqlen_k > 0 ? a.max_seqlen_k : 1) * a.Hkv * a.D * 4;
+    prm.band = static_cast<int>(std::max(1.0, std::min(static_cast<double>(a.S), 64.0 * (1 << 20) / kv_bytes)));
+    const long long bands = (a.S + prm.band - 1) / prm.band;
+    prm.n_items = bands * prm.band * prm.pairs * prm.row_blocks;
     prm.sched = sched_slot();
     if (!prm.sched) return cudaErrorInvalidDevice;
     prm.geom.block_size = a.block_size;
     prm.geom.shift = log2_if_pow2(a.block_size);
     prm.scale_log2 = a.scale * kLog2e;
-    return a.dtype == PA_BF16 ? launch_tc_typed<BF16>(prm, stream) : launch_tc_typed<F16>(prm, stream);
+    if (a.D == 64)
+        return a.dtype == PA_BF16 ? launch_tc_typed<BF16, 64>(prm, stream) : launch_tc_typed<F16, 64>(prm, stream);
+    return a.dtype == PA_BF16 ? launch_tc_typed<BF16, 128>(prm, stream) : launch_tc_typed<F16, 128>(prm, stream);
 }
 
 }  // namespace pa

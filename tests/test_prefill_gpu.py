@@ -67,7 +67,8 @@ def test_pool_path(orc, P, bs, causal):
 
 
 @pytest.mark.parametrize("G,D,dt", [(1, 64, "f16"), (2, 128, "f16"), (7, 64, "bf16"),
-                                    (4, 128, "bf16"), (8, 64, "f16")])
+                                    (4, 128, "bf16"), (8, 64, "f16"), (3, 128, "bf16"),
+                                    (5, 64, "f16")])
 def test_packed_path(orc, G, D, dt):
     Hkv = 2
     q_lens = [3, 64, 100, 129]
@@ -84,6 +85,21 @@ def test_packed_path(orc, G, D, dt):
                       block_size=16, scale=c.scale, dtype=dt)
     e = max_abs(f64(out), ref)
     assert e <= TOL[dt], e
+    assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("bs", [16, 4])
+def test_pool_path_qwen25_head_shape(orc, bs):
+    """The Qwen2.5-0.5B head shape (14 query / 2 kv heads, head dim 64: groups of 7, one pair
+    with a single head) with a cached prefix; 16-token blocks take the tcgen05 kernel, 4-token
+    blocks the mma.sync one."""
+    c = W.prefill_case(q_lens=[1, 63, 64, 65, 130, 257], prefix_len=48, Hq=14, Hkv=2, D=64,
+                       block_size=bs, dtype="f16", seed=40 + bs)
+    out, kc, vc, err = _run_pool(c)
+    ref, kref, vref = _ref_pool(orc, c)
+    assert np.array_equal(bits(kc), kref) and np.array_equal(bits(vc), vref)
+    e = max_abs(f64(out), ref)
+    assert e <= TOL["f16"], e
     assert int(err.item()) == 0
 
 
@@ -164,3 +180,34 @@ def test_full_prefill_workload_every_prompt(orc, full_prefill, part):
                       block_size=c.block_size, scale=c.scale, dtype=c.dtype)
     e = max_abs(o[a:b], ref)
     assert e <= TOL["bf16"], e
+
+
+@pytest.fixture(scope="module")
+def full_qwen25_prefill(orc):
+    """The qwen25_prefill workload (the Qwen2.5-0.5B head shape: 64 prompts, 512-token shared
+    prefix, 14/2 heads, head dim 64, 16-token blocks, fp16) in the bench's launch configuration."""
+    c = W.make("qwen25_prefill")
+    out, kc, vc, err = _run_pool(c)
+    kref, vref = orc.store_kv(c.k, c.v, c.k_cache, c.v_cache, c.slot_mapping)
+    return c, f64(out), bits(kc), bits(vc), int(err.item()), kref, vref
+
+
+def test_full_qwen25_prefill_store_and_errors(full_qwen25_prefill):
+    c, o, kc, vc, err, kref, vref = full_qwen25_prefill
+    assert err == 0
+    assert np.array_equal(kc, kref) and np.array_equal(vc, vref)
+    assert np.isfinite(o).all()
+
+
+@pytest.mark.parametrize("part", range(4))
+def test_full_qwen25_prefill_every_prompt(orc, full_qwen25_prefill, part):
+    """Every output row of all 64 prompts of the Qwen2.5-shaped prefill against the oracle."""
+    c, o, _, _, _, kref, vref = full_qwen25_prefill
+    s0, s1 = 16 * part, 16 * (part + 1)
+    a, b = int(c.cu_seqlens_q[s0]), int(c.cu_seqlens_q[s1])
+    ka = int(c.cu_seqlens_k[s0])
+    ref = orc.prefill(c.q[a:b], None, None, kref, vref, c.cu_seqlens_q[s0:s1 + 1] - a,
+                      c.cu_seqlens_k[s0:s1 + 1] - ka, c.block_tables[s0:s1], Hkv=c.Hkv,
+                      block_size=c.block_size, scale=c.scale, dtype=c.dtype)
+    e = max_abs(o[a:b], ref)
+    assert e <= TOL["f16"], e

@@ -23,7 +23,8 @@ raw 16-bit patterns (``uint16``), so both sides start from the same bits.
 
 The five named workloads mirror the five configurations of the paged-decode benchmark:
 ``tiny``, ``qwen25_05b_decode``, ``qwen3_06b_decode``, ``prefill_prefix`` and
-``longtail_decode``.
+``longtail_decode``. A sixth, ``qwen25_prefill``, is the prefill of the Qwen2.5-0.5B head shape
+(14/2 heads, head dim 64, 16-token blocks) with the same prompt mix as ``prefill_prefix``.
 """
 from __future__ import annotations
 
@@ -374,6 +375,11 @@ CONFIGS: dict[str, Workload] = {
         "Varlen causal prefill, 64 prompts q U[100,1024], shared 512-token cached prefix, "
         "16/8 heads, D 128, bs 256, bf16", 3,
         dict(S=64, prefix_len=512, Hq=16, Hkv=8, D=128, block_size=256, dtype=BF16)),
+    "qwen25_prefill": Workload(
+        "qwen25_prefill", "prefill",
+        "Qwen2.5-0.5B-shaped varlen causal prefill: 64 prompts q U[100,1024], shared 512-token "
+        "cached prefix, 14/2 heads, D 64, bs 16, fp16", 5,
+        dict(S=64, prefix_len=512, Hq=14, Hkv=2, D=64, block_size=16, dtype=F16)),
     "longtail_decode": Workload(
         "longtail_decode", "decode",
         "Max-batch long-tail decode: 512 seqs, ctx lognormal(median 2048, sigma 1) clipped "
@@ -390,7 +396,7 @@ def _lengths(name: str, seed: int, n: int | None = None) -> np.ndarray:
         return rng.integers(128, 2048, size=n or 32, endpoint=True)
     if name == "qwen3_06b_decode":
         return rng.integers(100, 4096, size=n or 256, endpoint=True)
-    if name == "prefill_prefix":
+    if name in ("prefill_prefix", "qwen25_prefill"):
         return rng.integers(100, 1024, size=n or 64, endpoint=True)
     if name == "longtail_decode":
         x = rng.lognormal(mean=math.log(2048.0), sigma=1.0, size=n or 512)
