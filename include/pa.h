@@ -108,7 +108,9 @@ size_t pa_decode_workspace_size(int B, int Hq, int Hkv, int D, int max_blocks_pe
  * pa_decode or pa_store_decode launch that used `workspace` (with these sizes) has completed, the
  * number of dynamic-tail units that launch ran: 0 when it kept one equal share per CTA. Read from
  * the launch's own record in the workspace with a synchronous 64-byte device-to-host copy.
- * Returns -1 for sizes pa_decode would reject, a NULL workspace or a failed copy.
+ * Returns -1 for sizes pa_decode would reject, a NULL workspace or a failed copy. Launches whose
+ * table holds at most 256 positions per sequence run the short-context kernel, which writes no
+ * record: for those the value read is whatever an earlier launch left.
  */
 int pa_decode_debug_tail_units(const void *workspace, int B, int Hq, int Hkv, int D,
                                int max_blocks_per_seq, int block_size);

@@ -1610,6 +1610,8 @@ int decode_debug_tail_units(const void *workspace, int B, int Hq, int Hkv, int D
 
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream) {
     if (a.B == 0) return cudaSuccess;
+    // short contexts: one CTA per pair, a chain of two memory round trips (decode_short.cu)
+    if (short_decode_supported(a)) return launch_decode_short(a, stream);
     DecodeParams prm{};
     // rows per TMA box: the largest power of two dividing both the block size and the tile
     int R = 1;

@@ -56,6 +56,10 @@ struct DecodeArgs {
     bool allow_wide = true;                           // see plan_decode
 };
 cudaError_t launch_decode(const DecodeArgs &a, const DecodePlan &plan, cudaStream_t stream);
+// short contexts (decode_short.cu): at most 256 positions per sequence by the table's width, one
+// CTA per (sequence, kv head), no workspace; launch_decode takes it when it applies
+bool short_decode_supported(const DecodeArgs &a);
+cudaError_t launch_decode_short(const DecodeArgs &a, cudaStream_t stream);
 // the dynamic-tail units (K2) of the last completed launch on this workspace (pa_decode's launch
 // configuration), read from unit 0's record; -1 on invalid sizes or a failed copy
 int decode_debug_tail_units(const void *workspace, int B, int Hq, int Hkv, int D,
