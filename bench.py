@@ -55,8 +55,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic (read + write bytes) of one launch, from the ncu captures of these kernels (layer 0
 # of the default workload; prefill_prefix; qwen25_prefill). Each is valid only for the kernel sources it was taken
 # on, identified by their hash; after any change the bench reports null.
-DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_289_356_032,
-                  "sha256": "1361a7dda18d1b40a99411ced40578b9055708f5be1b9b61207b8c3b496cd270"}
+DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_289_404_160,
+                  "sha256": "32d9050a51c21d042a5c2a0305b231dea999efc7c6625484aaf31d9639da8bb0"}
 STORE_TRAFFIC = {"sources": ("store_kv.cu", "pa_common.cuh"), "bytes": 218_096_128,
                  "sha256": "9940671f5a00740d1ba3ee485ac0d8bdb7dee7db79bbd1fe95feb25da0dc412c"}
 PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 419_378_688,
