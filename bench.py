@@ -331,10 +331,14 @@ def run_gpu(args, ws_, rank, local):
     bf16_peak = float(pk["bf16_tflops"])
     bf16_sustained = float(pk.get("bf16_tflops_sustained", bf16_peak))
 
-    if args.only == "prefill":
-        # the prefill rows alone (store + varlen prefill on the two prefill workloads): a short command for
-        # profiling those two kernels without the decode pools on the device
-        rows = bench_prefill(torch, pa, dev, stream, bf16_peak, bf16_sustained, hbm, args, pk_kind)
+    if args.only is not None:
+        # one group of rows alone: the prefill rows (store + varlen prefill on the two prefill
+        # workloads) or the small decode workloads as CUDA graphs; a short command for profiling
+        # their kernels without the headline's decode pools on the device
+        if args.only == "prefill":
+            rows = bench_prefill(torch, pa, dev, stream, bf16_peak, bf16_sustained, hbm, args, pk_kind)
+        else:
+            rows = {"decode_small_graphs": bench_small_decode(torch, pa, dev, hbm)}
         if rank == 0:
             print(json.dumps({"rows": rows}), flush=True)
         if dist is not None:
@@ -814,7 +818,7 @@ def main():
     ap.add_argument("--layers", type=int, default=2, help="layers whose pools alternate")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clock-tail", action="store_true")
-    ap.add_argument("--only", choices=["prefill"], default=None,
+    ap.add_argument("--only", choices=["prefill", "small"], default=None,
                     help="run one row alone (no headline line): for profiling its kernels")
     args = ap.parse_args()
     if args.warmup < 3:
