@@ -211,3 +211,28 @@ def test_full_qwen25_prefill_every_prompt(orc, full_qwen25_prefill, part):
                       block_size=c.block_size, scale=c.scale, dtype=c.dtype)
     e = max_abs(o[a:b], ref)
     assert e <= TOL["f16"], e
+
+
+def test_max_seqlen_k_only_orders_the_work(orc):
+    """max_seqlen_k sizes the bands of prompts the work goes out in (and nothing else): 0, 1, the
+    true bound and a huge value give bit-identical outputs (every item's arithmetic is the same
+    whichever CTA takes it), equal to the oracle."""
+    c = W.prefill_case(q_lens=[5, 130, 300, 64, 200, 17, 129, 256, 1, 77], prefix_len=256, Hq=16,
+                       Hkv=8, D=128, block_size=256, dtype="bf16", seed=77)
+    kc, vc = to_dev(c.k_cache, "bf16"), to_dev(c.v_cache, "bf16")
+    pa.pa_store_kv(to_dev(c.k, "bf16"), to_dev(c.v, "bf16"), kc, vc, i32(c.slot_mapping))
+    q = to_dev(c.q, "bf16")
+    outs = []
+    for hint in (c.max_seqlen_k, 0, 1, 1 << 30):
+        out = torch.empty_like(q)
+        err = err_buf()
+        pa.pa_prefill_varlen(out, q, None, None, kc, vc, i32(c.cu_seqlens_q), i32(c.cu_seqlens_k),
+                             c.max_seqlen_q, hint, i32(c.block_tables), Hkv=c.Hkv, scale=c.scale,
+                             err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs.append(bits(out))
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+    ref, _, _ = _ref_pool(orc, c)
+    o = f64(torch.from_numpy(outs[0].view(np.int16)).view(torch.bfloat16))
+    assert max_abs(o, ref) <= TOL["bf16"]

@@ -97,3 +97,23 @@ def test_prefill_config_structure():
         for r in (0, int(c.q_lens[s]) - 1):
             p = 512 + r
             assert slots[c.cu_seqlens_q[s] + r] == c.block_tables[s, p // 256] * 256 + p % 256
+
+
+def test_qwen25_prefill_config_structure():
+    """The Qwen2.5-shaped prefill: the prefill_prefix prompt mix at 14/2 heads, D 64, 16-token
+    blocks, fp16; the shared 512-token prefix is 32 blocks every prompt points at."""
+    c = W.make("qwen25_prefill", n=5)
+    assert (c.Hq, c.Hkv, c.D, c.block_size, c.dtype) == (14, 2, 64, 16, "f16")
+    assert (c.k_lens - c.q_lens == 512).all()
+    assert c.q_lens.min() >= 100 and c.q_lens.max() <= 1024
+    pre = c.block_tables[:, :32]
+    assert (pre == pre[0]).all() and len(set(pre[0].tolist())) == 32
+    assert (c.refcount[pre[0]] == 5).all()
+    slots = c.slot_mapping
+    assert len(set(slots.tolist())) == len(slots)
+    assert not (np.isin(slots // c.block_size, pre[0])).any()
+    for s in range(c.S):
+        for r in (0, int(c.q_lens[s]) - 1):
+            p = 512 + r
+            assert slots[c.cu_seqlens_q[s] + r] == c.block_tables[s, p // 16] * 16 + p % 16
+    assert np.array_equal(W.lengths("qwen25_prefill"), W.lengths("prefill_prefix", seed=5))
