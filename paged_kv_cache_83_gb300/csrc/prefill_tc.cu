@@ -10,7 +10,8 @@
 // of one GQA group, which share every K/V tile) from a counter until none is left, so the start-up
 // of one item overlaps the end of the previous one. Head dim 64 or 128 (one or two 64-column halves
 // per tile); a group of G query heads is cut into ceil(G / 2) pairs, and the pair that has one head
-// (odd G) computes its second head on a zero Q tile whose output is dropped.
+// (odd G) computes its second head on a zero Q tile whose output is dropped. Items go out in bands
+// of prompts whose K/V fits in L2 (sized from max_seqlen_k), largest first within a band.
 //
 //   warp 3      scheduler: claims items, reads their lengths, checks the block table, drops items
 //               without rows, writes zero rows + an error bit for bad ones, and queues the rest.
@@ -28,8 +29,8 @@
 //               memory in the swizzled layout the PV MMA reads. O is rescaled in TMEM only when
 //               the row max grew by more than 2^8 (the normaliser uses the same reference, so the
 //               result is exact). The output rows leave through the warp's rows of the P buffer
-//               as whole 256-byte rows.
-//   TMEM columns: S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511.
+//               as whole rows (D * 2 bytes).
+//   TMEM columns: S_A 0-127, S_B 128-255, O_A from 256, O_B from 384 (D columns each).
 // Every wait is bounded (PA_DEVERR_TIMEOUT); on a timeout every role drains what it started
 // (TMA, MMAs) before the TMEM is freed.
 #include <cuda.h>
