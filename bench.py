@@ -59,10 +59,10 @@ DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_289_404_
                   "sha256": "32d9050a51c21d042a5c2a0305b231dea999efc7c6625484aaf31d9639da8bb0"}
 STORE_TRAFFIC = {"sources": ("store_kv.cu", "pa_common.cuh"), "bytes": 218_096_128,
                  "sha256": "9940671f5a00740d1ba3ee485ac0d8bdb7dee7db79bbd1fe95feb25da0dc412c"}
-PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 419_535_360,
-                   "sha256": "0ac64420bf80f33041f751f7fe3722c2c876141c8900f4fdef29c3129b76840d"}
-PREFILL_QWEN25_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 111_493_376,
-                          "sha256": "0ac64420bf80f33041f751f7fe3722c2c876141c8900f4fdef29c3129b76840d"}
+PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 420_153_088,
+                   "sha256": "b60f77030b2520ca11a812a08ca2289372d29864ea0efe5cf34843ce1e3795b0"}
+PREFILL_QWEN25_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 111_261_952,
+                          "sha256": "b60f77030b2520ca11a812a08ca2289372d29864ea0efe5cf34843ce1e3795b0"}
 
 
 def peaks() -> tuple[dict, str]:

@@ -20,17 +20,21 @@
 //               3-slot ring in the order the MMAs consume them (K0, K1, V0, K2, V1, ...).
 //   warps 1, 2  one MMA issuer per head (one thread each; warp 1 owns the 512 TMEM columns):
 //                 S_h = Q_h K^T   as soon as the softmax has read S_h of the previous tile,
-//                 O_h += P_h V    as soon as P_h is in shared memory.
-//               Both operands of both MMAs come from shared memory, so S of the next tile (or the
-//               next item's first tile) is computed while the softmax still works on the current one.
+//                 O_h += P_h V    as soon as P_h is written.
+//               Q, K and V come from shared memory, and P never shares columns with S, so S of the
+//               next tile (or the next item's first tile) is computed while the softmax still works
+//               on the current one.
 //   warps 4-7   softmax of head A, warps 8-11 softmax of head B: thread = one query row = one
 //               TMEM lane. S is read once into registers (then released), masked (causal bound
-//               P + row, context end), row max, P = 2^(s - m) in bf16/fp16 stored to shared
-//               memory in the swizzled layout the PV MMA reads. O is rescaled in TMEM only when
+//               P + row, context end), row max, P = 2^(s - m) in bf16/fp16: at head dim 128
+//               stored to shared memory in the swizzled layout the PV MMA reads, at head dim 64
+//               written to TMEM columns of its own (the PV MMA's A operand; the row's P leaves the
+//               shared-memory store port alone, 8 % faster there). O is rescaled in TMEM only when
 //               the row max grew by more than 2^8 (the normaliser uses the same reference, so the
 //               result is exact). The output rows leave through the warp's rows of the P buffer
 //               as whole rows (D * 2 bytes).
-//   TMEM columns: S_A 0-127, S_B 128-255, O_A from 256, O_B from 384 (D columns each).
+//   TMEM columns: S_A 0-127, S_B 128-255, O_A from 256, O_B from 384 (D columns each); at head
+//   dim 64 P_A 320-383 and P_B 448-511 (16-bit pairs, one row per lane).
 // Every wait is bounded (PA_DEVERR_TIMEOUT); on a timeout every role drains what it started
 // (TMA, MMAs) before the TMEM is freed.
 #include <cuda.h>
@@ -49,7 +53,8 @@ namespace {
 constexpr int BM = 128, BN = 128;
 constexpr int kThreads = 384;
 constexpr int kHalf = BM * 64 * 2;  // one 128-row x 64-column half tile: 16 KB
-constexpr int kPTile = BM * BN * 2; // P (128 rows x 128 keys): 32 KB, also the output stage
+constexpr int kPTile = BM * BN * 2; // P (128 rows x 128 keys): 32 KB, also the output stage (the
+                                    // output stage alone at head dim 64, where P is in TMEM)
 constexpr int kRing = 3;            // K/V tile slots
 // per-head barriers take index base + h (h = 0 for head A, 1 for head B)
 enum {
@@ -59,7 +64,7 @@ enum {
     B_EMPTY = B_FULL + kRing,  // + slot: both heads' MMAs are done with it (two commits)
     B_S = B_EMPTY + kRing,     // + h: S = Q K^T is in TMEM
     B_F = B_S + 2,             // + h: the softmax warps have read S (4 arrivals)
-    B_P = B_F + 2,             // + h: P is in shared memory (4 arrivals)
+    B_P = B_F + 2,             // + h: P is written (4 arrivals)
     B_O = B_P + 2,             // + h: O += P V is done, so P's buffer is free again
     B_OFREE = B_O + 2,         // + h: the item's output has been read out of TMEM (4 arrivals)
     B_END = B_OFREE + 2,       // + h: every MMA of that head has completed
@@ -112,6 +117,14 @@ __device__ __forceinline__ bool tc_warp_wait(uint32_t bar, uint32_t parity, vola
     return all;
 }
 
+// 4 consecutive 32-bit TMEM columns of this thread's lane (a 4-register operand: the 16-register
+// form of the same store made the softmax spill at the 168-register limit)
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b),
+                 "r"(c), "r"(d)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tc_abort(int32_t *err, volatile int *abort_flag) {
     raise_err(err, PA_DEVERR_TIMEOUT);
     *abort_flag = 1;
@@ -131,6 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                   OFF_RING = Lay::OFF_RING, OFF_BAR = Lay::OFF_BAR, OFF_ITEMS = Lay::OFF_ITEMS,
                   OFF_MISC = Lay::OFF_MISC;
     constexpr int kHalves = Lay::kHalves;
+    // head dim 64: P has TMEM columns of its own (S 0-255, O_A 256-319, P_A 320-383, O_B 384-447,
+    // P_B 448-511), so the softmax writes it with tcgen05.st and PV reads it as the A operand
+    constexpr bool kPTmem = HD == 64;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_addr(smem);
@@ -336,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const uint64_t dk0 = smem_desc_sw128(sbase + OFF_RING, 16, 1024);
         const uint64_t dv0 = smem_desc_sw128(sbase + OFF_RING, kHalf, 1024);
         const uint32_t s_tm = tmem + (h ? 128 : 0), o_tm = tmem + 256 + (h ? 128 : 0);
+        const uint32_t p_tm = tmem + 256 + HD + (h ? 128 : 0);  // P in TMEM (head dim 64)
         auto qk = [&](int slot) {  // S = Q K^T: A = Q (K-major), B = K rows (K-major)
             const uint64_t kb = dk0 + slot * Lay::kKVDesc;
 #pragma unroll
@@ -349,7 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
                 const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                tc_mma_ss(o_tm, dp + off, vb + ((kk * 2048) >> 4), IPV, (acc || kk > 0));
+                if constexpr (kPTmem)
+                    tc_mma_ts(o_tm, p_tm + kk * 8, vb + ((kk * 2048) >> 4), IPV, (acc || kk > 0));
+                else
+                    tc_mma_ss(o_tm, dp + off, vb + ((kk * 2048) >> 4), IPV, (acc || kk > 0));
             }
         };
         long long ci = 0;  // loads consumed
@@ -459,7 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t srow = tmem + lane_off + (h ? 128 : 0);
         const uint32_t orow = tmem + lane_off + 256 + (h ? 128 : 0);
-        unsigned char *prow = smem + (h ? OFF_PB : OFF_PA) + r * 128;  // this row of P, half 0
+        // this row of P (half 0) in shared memory; with P in TMEM it serves the output stage only
+        auto prow_of = [&]() { return smem + (h ? OFF_PB : OFF_PA) + r * 128; };
         const uint32_t s_full = bar(B_S + h), s_free = bar(B_F + h), p_full = bar(B_P + h);
         const uint32_t o_done = bar(B_O + h), o_free = bar(B_OFREE + h);
         long long t = 0;  // tiles of this head so far
@@ -517,17 +538,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     if (!(ok = tc_warp_wait(o_done, static_cast<uint32_t>((t - 1) & 1), abort_flag))) break;
                     tc_fence_after();
                 }
-                // P row r: 16-byte chunk q of half q / 8 sits at chunk (q % 8) ^ (r % 8) of the
-                // 128-byte row (the 128-byte swizzle the MMA descriptor names). The warp's rows
-                // may still be the source of the previous item's output store.
-                if (j == 0) {
-                    if (lane == 0) bulk_wait_read();
-                    __syncwarp();
-                }
+                if constexpr (kPTmem) {
+                    // P in its own TMEM columns (the A operand of the PV MMA)
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    *reinterpret_cast<uint4 *>(prow + (q >> 3) * kHalf + (((q & 7) ^ (r & 7)) << 4)) =
-                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    for (int c = 0; c < 16; ++c)
+                        tmem_st4(orow + HD + 4 * c, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    tmem_wait_st();
+                } else {
+                    // P row r: 16-byte chunk q of half q / 8 sits at chunk (q % 8) ^ (r % 8) of the
+                    // 128-byte row (the 128-byte swizzle the MMA descriptor names). The warp's rows
+                    // may still be the source of the previous item's output store.
+                    if (j == 0) {
+                        if (lane == 0) bulk_wait_read();
+                        __syncwarp();
+                    }
+                    unsigned char *prow = prow_of();
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        *reinterpret_cast<uint4 *>(prow + (q >> 3) * kHalf + (((q & 7) ^ (r & 7)) << 4)) =
+                            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
                 // O(t - 1) is complete: rescale it before this tile's PV adds to it
                 if (j > 0 && __any_sync(kFull, need)) {
 #pragma unroll
@@ -541,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     }
                     tmem_wait_st();
                 }
-                fence_proxy_async_smem();
+                if constexpr (!kPTmem) fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full);
@@ -566,6 +596,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             if (lane == 0) mbar_arrive(o_free);
             // The warp's 32 rows go out through their own rows of the P buffer (swizzled like P):
             // two TMA stores when all 32 rows belong to the item, else row-wide 16-byte stores.
+            // With P in TMEM nothing else has waited for the previous item's store to read them.
+            if constexpr (kPTmem) {
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
+            }
+            unsigned char *prow = prow_of();
 #pragma unroll
             for (int c = 0; c < HD / 8; ++c)
                 *reinterpret_cast<uint4 *>(prow + (c >> 3) * kHalf + (((c & 7) ^ (r & 7)) << 4)) =
