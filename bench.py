@@ -10,8 +10,9 @@ Headline: KV bytes the step must read (every cached row of K and V once per kv h
 by the device time of the step, in GB/s, and as a fraction of the measured HBM peak; decode
 steps per second per layer. The same line carries:
 
-* ``roofline``: the step's call (split kernel + merge) timed alone with CUDA events inside
-  the timed region, against the measured copy bandwidth;
+* ``roofline``: the step's call (split kernel + merge): its mean duration over the timed region
+  (the events around the K steps; each step is exactly this call, and no event between steps
+  holds a launch back from overlapping the one before), against the measured copy bandwidth;
 * ``e2e``: the same metric through the C-ABI's host-buffer call (pa_store_decode_host): every
   step copies its inputs from pinned host memory and reads the output back, synchronising each
   step (the pool stays resident, as in an engine);
@@ -359,16 +360,11 @@ def run_gpu(args, ws_, rank, local):
     launches_per_step = 1 + (1 if plan_splits else 0)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
-    dec_ev = [(ev(), ev()) for _ in range(args.steps)]
 
-    def step(i, timed=False):
+    def step(i):
         L = layers[i % nl]
-        if timed:
-            dec_ev[i][0].record(stream)
         pa.pa_store_decode(L.out, L.q, L.k_new, L.v_new, L.kc, L.vc, L.bt, L.cl, L.c.scale,
                            workspace=L.ws)
-        if timed:
-            dec_ev[i][1].record(stream)
 
     def barrier():
         if dist is not None:
@@ -383,7 +379,7 @@ def run_gpu(args, ws_, rank, local):
     t0, t1 = ev(), ev()
     t0.record(stream)
     for i in range(args.steps):
-        step(i, timed=True)
+        step(i)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -399,7 +395,8 @@ def run_gpu(args, ws_, rank, local):
     clk = clocks.stop()
 
     elapsed = t0.elapsed_time(t1)  # ms
-    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
+    # this rank's mean call: the steps run back to back, one pa_store_decode each
+    dec_mean = elapsed / args.steps
     # the same step as two calls (pa_store_kv, then pa_decode), for comparison
     n2 = max(3, min(args.steps, 200))
     st_ev = [(ev(), ev(), ev()) for _ in range(n2)]
@@ -418,7 +415,6 @@ def run_gpu(args, ws_, rank, local):
     ms_step = elapsed / args.steps
     step_bytes = sum(nbytes[i % nl] for i in range(args.steps))
     value = weak_gbs(ws_, step_bytes, elapsed)
-    dec_mean = statistics.mean(dec_ms)
     dec_bytes_mean = statistics.mean(nbytes[i % nl] for i in range(args.steps))
     achieved = dec_bytes_mean / (dec_mean * 1e-3) / 1e9
     # traffic was captured on layer 0; report it for the launches on that layer
@@ -637,7 +633,9 @@ GROUP_SWEEP = ((4, 4, 128, 256, "bf16"), (7, 2, 64, 16, "f16"), (8, 2, 128, 256,
 def bench_group_sweep(torch, pa, dev, hbm) -> dict:
     """pa_decode across GQA group sizes G = Hq / Hkv (G >= 4 runs the tensor-core consumers).
     Like the main step: calls back to back on two layers whose pools alternate (each KV set is
-    larger than L2), CUDA events around each call, the median call reported."""
+    larger than L2), one pair of CUDA events around the n calls, the mean call reported. (An event
+    between two calls would hold the next decode launch until the previous merge has finished,
+    which no step loop does: 2-3 µs a call.)"""
     res = {}
     for G, Hkv, D, bs, dt in GROUP_SWEEP:
         lens = np.random.default_rng(0).integers(100, 4096, size=256, endpoint=True)
@@ -652,14 +650,14 @@ def bench_group_sweep(torch, pa, dev, hbm) -> dict:
         for i in range(4):
             run(layers[i % 2])
         n = 20
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        e0.record()
         for i in range(n):
-            evs[i][0].record()
             run(layers[i % 2])
-            evs[i][1].record()
+        e1.record()
         torch.cuda.synchronize()
-        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+        ms = e0.elapsed_time(e1) / n
         kv = kv_bytes(c.context_lens, c.Hkv, c.D)
         res[f"G{G}_Hkv{Hkv}_D{D}_bs{bs}_{dt}"] = {
             "us": ms * 1e3, "kv_bytes": kv, "GB_per_s": kv / (ms * 1e-3) / 1e9,
@@ -673,7 +671,8 @@ def bench_group_sweep(torch, pa, dev, hbm) -> dict:
 def bench_longtail(torch, pa, dev, hbm) -> dict:
     """The max-batch long-tail decode workload (512 sequences, lognormal contexts up to 16384, a
     near-full pool): the same step as the headline (pa_store_decode), calls back to back on one
-    layer whose 6.8 GB KV set is far larger than L2; the median call reported."""
+    layer whose 6.8 GB KV set is far larger than L2, one pair of CUDA events around the n calls;
+    the mean call reported."""
     c = W.make("longtail_decode")
     L = DecodeLayer(torch, pa, c, dev)
 
@@ -683,14 +682,14 @@ def bench_longtail(torch, pa, dev, hbm) -> dict:
     for _ in range(3):
         run()
     n = 10
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    for a, b in evs:
-        a.record()
+    e0.record()
+    for _ in range(n):
         run()
-        b.record()
+    e1.record()
     torch.cuda.synchronize()
-    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    ms = e0.elapsed_time(e1) / n
     kv = kv_bytes(c.context_lens, c.Hkv, c.D)
     res = {"workload": "longtail_decode", "seqs": c.B, "kv_bytes": kv, "ms": ms,
            "GB_per_s": kv / (ms * 1e-3) / 1e9, "frac_of_hbm": kv / (ms * 1e-3) / 1e9 / hbm,
@@ -736,7 +735,7 @@ def bench_block_manager(pa) -> dict:
 
 
 def time_prefill(torch, pa, dev, stream, name, steps):
-    """Store + varlen prefill of one prefill workload, L2 flushed before each iteration: the mean
+    """Store + varlen prefill of one prefill workload, L2 flushed before each iteration: the median
     CUDA-event times (ms) of the store and of the prefill, and the case."""
     c = W.make(name)
     i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
@@ -766,10 +765,13 @@ def time_prefill(torch, pa, dev, stream, name, steps):
     torch.cuda.synchronize()
     for e in evs:
         torch.amax(flush)  # L2 flush between iterations (outside the events)
+        # a bounded on-device wait (outside the events) while the host queues the timed calls, so
+        # that a host stall cannot put launch latency between the first event and the store
+        torch.cuda._sleep(200_000)
         run(e)
     torch.cuda.synchronize()
-    st = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    pf = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    st = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    pf = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
     return st, pf, c
 
 
