@@ -60,10 +60,10 @@ DECODE_TRAFFIC = {"sources": ("decode.cu", "pa_common.cuh"), "bytes": 2_289_404_
                   "sha256": "32d9050a51c21d042a5c2a0305b231dea999efc7c6625484aaf31d9639da8bb0"}
 STORE_TRAFFIC = {"sources": ("store_kv.cu", "pa_common.cuh"), "bytes": 218_096_128,
                  "sha256": "9940671f5a00740d1ba3ee485ac0d8bdb7dee7db79bbd1fe95feb25da0dc412c"}
-PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 420_153_088,
-                   "sha256": "b60f77030b2520ca11a812a08ca2289372d29864ea0efe5cf34843ce1e3795b0"}
-PREFILL_QWEN25_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 111_261_952,
-                          "sha256": "b60f77030b2520ca11a812a08ca2289372d29864ea0efe5cf34843ce1e3795b0"}
+PREFILL_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 418_674_432,
+                   "sha256": "d665bf6dcb2d3691c3698422946b45614298a0afd57c138209ca60fe9fdeb949"}
+PREFILL_QWEN25_TRAFFIC = {"sources": ("prefill_tc.cu", "pa_common.cuh"), "bytes": 111_464_960,
+                          "sha256": "d665bf6dcb2d3691c3698422946b45614298a0afd57c138209ca60fe9fdeb949"}
 
 
 def peaks() -> tuple[dict, str]:

@@ -69,7 +69,9 @@ enum {
     B_OFREE = B_O + 2,         // + h: the item's output has been read out of TMEM (4 arrivals)
     B_END = B_OFREE + 2,       // + h: every MMA of that head has completed
     B_VZ = B_END + 2,          // the last V tile's rows past the keys are zero
-    B_IFULL = B_VZ + 1,        // + k: work item k of the queue is published
+    B_VZACK,                   // head B has waited for that zeroing (so head A never runs two
+                               // zeroings ahead of it: a parity wait cannot tell those apart)
+    B_IFULL = B_VZACK + 1,     // + k: work item k of the queue is published
     B_IEMPTY = B_IFULL + 2,    // + k: every role has read it (kItemReaders arrivals)
     NBAR = B_IEMPTY + 2
 };
@@ -432,6 +434,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 // The last tile may hold rows past the keys (unwritten slots or another prompt):
                 // zero them before any PV reads them (P is zero there, but 0 * NaN is not).
                 if (h == 0) {
+                    if (zt > 0 && !(ok = tc_warp_wait(bar(B_VZACK), static_cast<uint32_t>((zt - 1) & 1), abort_flag)))
+                        break;
                     unsigned char *vt = smem + OFF_RING + slot * Lay::kKV;
                     for (int c = lane; c < (BN - last_valid) * (HD / 8); c += 32) {  // 16-byte chunks
                         const int r = last_valid + c / (HD / 8), c16 = c % (HD / 8);
@@ -441,8 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(B_VZ));
-                } else if (!(ok = tc_warp_wait(bar(B_VZ), zt & 1, abort_flag))) {
-                    break;
+                } else {
+                    if (!(ok = tc_warp_wait(bar(B_VZ), zt & 1, abort_flag))) break;
+                    if (lane == 0) mbar_arrive(bar(B_VZACK));
                 }
                 ++zt;
             }
