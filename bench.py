@@ -763,11 +763,14 @@ def time_prefill(torch, pa, dev, stream, name, steps):
     n = max(3, min(steps, 50))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
     torch.cuda.synchronize()
+    # a bounded on-device wait (outside the events) while the host queues the timed calls, so
+    # that a host stall cannot put launch latency between the first event and the store (a private
+    # torch helper: without it the calls are timed as they come)
+    gpu_sleep = getattr(torch.cuda, "_sleep", None)
     for e in evs:
         torch.amax(flush)  # L2 flush between iterations (outside the events)
-        # a bounded on-device wait (outside the events) while the host queues the timed calls, so
-        # that a host stall cannot put launch latency between the first event and the store
-        torch.cuda._sleep(200_000)
+        if gpu_sleep is not None:
+            gpu_sleep(200_000)
         run(e)
     torch.cuda.synchronize()
     st = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
